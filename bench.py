@@ -1,0 +1,350 @@
+#!/usr/bin/env python
+"""Benchmark: Ozaki Scheme II emulated DGEMM on GB300 (one process per GPU).
+
+One step = one pass of the whole Scheme II path (exponents -> residue split ->
+per-modulus exact GEMM -> CRT + rounding) over m = n = k = 16384 with s = 14 moduli
+on HPL-like phi = 0.5 inputs, through the library's C ABI with the inputs resident
+in HBM.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the CPU oracle (the plain restatement of the method in
+``oracle/``) on the host cores, on a bounded sample of the same workload.
+Multi-GPU: the path does not shard; N ranks run N independent replicas and the
+value is the total over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "emulated FP64 TFLOPS at 16384³ (s=14) and % of INT8 tensor-core roofline"
+UNIT = "TFLOPS"
+M = N = K = 16384
+S = 14
+PHI = 0.5
+SEED = 0
+PAGES_GH200_TFLOPS = 80.2  # the pages' Scheme II figure at 16384^3, s=14 (GH200): context
+KERNELS_PER_STEP = 6       # rowexp, colexp, split(A), split(B), residue GEMM, CRT
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    """Max over ranks (the slowest rank decides the job time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+    from oracle import ozaki2 as O
+
+    ms, ns = 128, 128  # sample: a 128 x 128 block of C with the full k = 16384
+    A, B = hpl_like(ms, ns, K, phi=PHI, seed=SEED)
+    times = []
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        O.ozaki2_dgemm(A, B, S, keep=False)
+        if it >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2.0 * ms * ns * K * len(times) / total / 1e12
+    cores = os.cpu_count()
+    sample = f"oracle ozaki2_dgemm on a {ms}x{ns}x{K} block (s={S}, phi={PHI}); float64 BLAS matmul per modulus"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"ozaki2_dgemm m=n=k={M} s={S} phi={PHI} (sampled {ms}x{ns}x{K} block)",
+                   "m": M, "n": N, "k": K, "moduli": S, "phi": PHI, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def cpu_baseline_measure():
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+    from oracle import ozaki2 as O
+
+    ms, ns = 256, 256
+    A, B = hpl_like(ms, ns, K, phi=PHI, seed=SEED)
+    t0 = time.perf_counter()
+    O.ozaki2_dgemm(A, B, S, keep=False)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * ms * ns * K / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"one oracle ozaki2_dgemm on a {ms}x{ns}x{K} block of the workload (s={S}, phi={PHI}), "
+                      f"{dt:.1f} s; numpy float64 BLAS for the per-modulus products, Python integers for the CRT"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from fp64_gemm_emulation_gb300 import ozaki as oz
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+
+    peaks, peak_src = load_peaks()
+    lib = oz._lib
+    A_np, B_np = hpl_like(M, N, K, phi=PHI, seed=SEED)
+    dA = torch.from_numpy(A_np.T.copy()).to(device).t()
+    dB = torch.from_numpy(B_np.T.copy()).to(device).t()
+    dC = torch.empty((N, M), dtype=torch.float64, device=device).t()
+    mp, np_, kp = oz.ozaki2_plane_dims(M, N, K)
+    rowexp = torch.empty(M, dtype=torch.int32, device=device)
+    colexp = torch.empty(N, dtype=torch.int32, device=device)
+    Ap = torch.empty((S, mp, kp), dtype=torch.int16, device=device)
+    Bp = torch.empty((S, np_, kp), dtype=torch.int16, device=device)
+    Cr = torch.empty((S, np_, mp), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sh = stream.cuda_stream
+    ptr = lambda t: t.data_ptr()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        rc = lib.ozaki2_exponents(M, N, K, ptr(dA), M, ptr(dB), K, ptr(rowexp), ptr(colexp), sh)
+        if ev:
+            ev[1].record(stream)
+        rc |= lib.ozaki2_split(M, N, K, ptr(dA), M, ptr(dB), K, S, ptr(rowexp), ptr(colexp), ptr(Ap), ptr(Bp), sh)
+        if ev:
+            ev[2].record(stream)
+        rc |= lib.ozaki2_residue_gemm(M, N, K, S, ptr(Ap), ptr(Bp), ptr(Cr), sh)
+        if ev:
+            ev[3].record(stream)
+        rc |= lib.ozaki2_crt(M, N, K, S, ptr(Cr), ptr(rowexp), ptr(colexp), ptr(dC), M, sh)
+        if ev:
+            ev[4].record(stream)
+        if rc:
+            raise RuntimeError(f"ozaki call failed: {rc}")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clk = clocks.stop()
+    status = oz.ozaki_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    elapsed_ms = start.elapsed_time(end)
+    phase_ms = np.zeros(4)
+    for e in evs:
+        for p in range(4):
+            phase_ms[p] += e[p].elapsed_time(e[p + 1])
+    phase_ms /= args.steps
+    job_ms = reduce_max(elapsed_ms, world, device)
+    flops = 2.0 * M * N * K
+    value = world * flops * args.steps / (job_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (the residue GEMM), per launch
+    gemm_ms = phase_ms[2]
+    int_ops = S * 2.0 * M * N * K
+    peak_t = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved = int_ops / (gemm_ms * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("residue_gemm_16384_s14_bytes_per_launch")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                "frac": achieved / peak_t, "traffic": traffic,
+                "kernel": "oz::residue_gemm_kernel (s x 2mnk exact integer products on tcgen05 BF16)",
+                "peak_source": f"{peak_src} bf16 dense, sustained (kernel timed inside a long step)"}
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    split_bytes = 8.0 * (M * K + K * N) + 2.0 * S * (mp * kp + np_ * kp)
+    phases = {
+        "exponents_ms": phase_ms[0], "split_ms": phase_ms[1], "gemm_ms": phase_ms[2], "crt_ms": phase_ms[3],
+        "exponents_hbm_frac": 8.0 * (M * K + K * N) / (phase_ms[0] * 1e-3) / 1e9 / hbm,
+        "split_hbm_frac": split_bytes / (phase_ms[1] * 1e-3) / 1e9 / hbm,
+        "crt_hbm_frac": (S * 1.0 * mp * np_ + 8.0 * M * N) / (phase_ms[3] * 1e-3) / 1e9 / hbm,
+        "non_gemm_share": float((phase_ms.sum() - phase_ms[2]) / phase_ms.sum()),
+        "gemm_frac_of_b200_int8_spec_4500": achieved / 4500.0,
+    }
+
+    # ---- end to end through the C ABI with pinned HOST buffers
+    hA = torch.from_numpy(A_np.T.copy()).pin_memory()   # column-major A as a (k, m) row-major block
+    hB = torch.from_numpy(B_np.T.copy()).pin_memory()
+    hC = torch.empty((N, M), dtype=torch.float64).pin_memory()
+    e2e_steps = max(1, min(args.steps, 3))
+    oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)  # warm-up
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)
+    e2e_s = reduce_max(time.perf_counter() - t0, world, device)
+    barrier(world)
+    e2e = {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 8 * (M * K + K * N), "d2h_bytes_per_step": 8 * M * N,
+           "api": "ozaki2_dgemm_host (pinned host A, B, C; copies inside the timed region)"}
+
+    # ---- context: native FP64 GEMM (cuBLAS through torch) on the same GPU, one call
+    context = {}
+    if rank == 0 and not args.no_context:
+        x = dA.contiguous()
+        y = dB.contiguous()
+        torch.matmul(x[:2048, :2048], y[:2048, :2048])
+        torch.cuda.synchronize(device)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        torch.matmul(x, y)
+        s1.record(stream)
+        torch.cuda.synchronize(device)
+        context["cublas_dgemm_tflops"] = flops / (s0.elapsed_time(s1) * 1e-3) / 1e12
+        del x, y
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": job_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": value / PAGES_GH200_TFLOPS, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"ozaki2_dgemm m=n=k={M} s={S} phi={PHI} (HPL-like, seed {SEED})",
+                       "m": M, "n": N, "k": K, "moduli": S, "phi": PHI,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "no flush: inputs (2 GiB each) and planes are far larger than L2"},
+            "roofline": roofline, "phases": phases, "e2e": e2e,
+            "cpu_baseline": cpu_baseline_measure() if not args.no_cpu_baseline else None,
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clk, "context": context,
+            "tensor_path": "residues in bf16, exact FP32 accumulation in TMEM, folded mod m_t every 960 k",
+            "vs_baseline_ref": "pages' GH200 Scheme II figure, 80.2 TFLOPS (other hardware)",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+// oz_crt.cu -- steps a5 + a6: CRT accumulation, range reduction, one rounding.
+//
+// [Ozaki II] Algorithm 1, steps 4-6.  Per output element, with residues
+// c_t = C''_t in [0, m_t) and P_t = M_t y_t (< M, so P_t / M = y_t / m_t):
+//   Z    = sum_t c_t P_t                      exact, six 32-bit limbs
+//   Q    = nearest integer to Z / M           from sum_t c_t floor(2^32 y_t / m_t)
+//   C''' = Z - Q M, then one correction by M  symmetric representative, |C'''| < M/2
+//   C    = RN(C''' 2^-(d_i + e_j))            one rounding, subnormals included
+// The quotient estimate errs by less than 1.3e-6, so it is off by at most one and the
+// single correction restores the unique representative ([Ozaki II] section 5: the
+// true product lies in (-M/2, M/2) because 2 c_max < M).  Integer arithmetic only.
+#include "oz_internal.h"
+
+namespace oz {
+
+// Bits [pos, pos + 64) of a 6-limb little-endian integer (zero beyond the top).
+__device__ __forceinline__ uint64_t window64(const uint32_t (&x)[kLimbs], int pos) {
+  const int li = pos >> 5, sh = pos & 31;
+  uint32_t a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+  for (int l = 0; l < kLimbs; ++l) {
+    a0 = (l == li) ? x[l] : a0;
+    a1 = (l == li + 1) ? x[l] : a1;
+    a2 = (l == li + 2) ? x[l] : a2;
+  }
+  const uint64_t lo = (static_cast<uint64_t>(a1) << 32) | a0;
+  return sh ? ((lo >> sh) | (static_cast<uint64_t>(a2) << (64 - sh))) : lo;
+}
+
+// True if any bit below position pos (pos >= 0) is set.
+__device__ __forceinline__ bool any_below(const uint32_t (&x)[kLimbs], int pos) {
+  bool any = false;
+#pragma unroll
+  for (int l = 0; l < kLimbs; ++l) {
+    const int lo = 32 * l;
+    if (lo + 32 <= pos)
+      any |= (x[l] != 0);
+    else if (lo < pos)
+      any |= (x[l] & ((1u << (pos - lo)) - 1u)) != 0;
+  }
+  return any;
+}
+
+// RN-even of (-1)^neg * mag * 2^-D as IEEE-754 binary64 bits.
+__device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLimbs], bool neg, int D) {
+  int L = 0;  // bit length of mag
+#pragma unroll
+  for (int l = 0; l < kLimbs; ++l)
+    if (mag[l] != 0) L = 32 * l + (32 - __clz(mag[l]));
+  if (L == 0) return 0;  // exact zero: +0.0
+  const int drop = max(L - 53, D - 1074);  // bits of mag below the result's last place
+  uint64_t mant;
+  if (drop <= 0) {
+    const uint64_t v = (static_cast<uint64_t>(mag[1]) << 32) | mag[0];  // L <= 53 here
+    mant = v << (-drop);
+  } else {
+    mant = window64(mag, drop);
+    const bool round = (window64(mag, drop - 1) & 1u) != 0;
+    const bool sticky = any_below(mag, drop - 1);
+    if (round && (sticky || (mant & 1u))) ++mant;
+  }
+  int e = drop - D;  // value = mant * 2^e
+  if (mant >= (1ull << 53)) {
+    mant >>= 1;
+    ++e;
+  }
+  uint64_t bits;
+  if (mant == 0) {
+    bits = 0;
+  } else if (mant >= (1ull << 52)) {
+    const int biased = e + 52 + 1023;
+    bits = (biased >= 2047) ? 0x7FF0000000000000ull
+                            : ((static_cast<uint64_t>(biased) << 52) | (mant & ((1ull << 52) - 1)));
+  } else {
+    bits = mant;  // subnormal: e == -1074
+  }
+  return bits | (neg ? 0x8000000000000000ull : 0ull);
+}
+
+__global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c,
+                                                  const uint8_t* __restrict__ C_res,
+                                                  const int32_t* __restrict__ rowexp,
+                                                  const int32_t* __restrict__ colexp, double* __restrict__ C,
+                                                  long long ldc) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m) return;
+  const long long plane = static_cast<long long>(np) * mp;
+  const int E = __ldg(rowexp + i);
+  for (int j = blockIdx.y; j < n; j += gridDim.y) {
+    const int F = __ldg(colexp + j);
+    double* out = C + i + j * ldc;
+    if (E == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) {
+      *out = __longlong_as_double(0x7FF8000000000000ll);
+      continue;
+    }
+    if (E == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) {
+      *out = 0.0;
+      continue;
+    }
+    uint64_t acc[kLimbs];
+#pragma unroll
+    for (int l = 0; l < kLimbs; ++l) acc[l] = 0;
+    uint64_t qs = 0;
+    const uint8_t* res = C_res + static_cast<long long>(j) * mp + i;
+#pragma unroll 4
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t r = __ldg(res + t * plane);
+#pragma unroll
+      for (int l = 0; l < kLimbs; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
+      qs += static_cast<uint64_t>(r) * c.frac[t];
+    }
+    // Z in 32-bit limbs
+    uint32_t z[kLimbs];
+    uint64_t carry = 0;
+#pragma unroll
+    for (int l = 0; l < kLimbs; ++l) {
+      const uint64_t v = acc[l] + carry;
+      z[l] = static_cast<uint32_t>(v);
+      carry = v >> 32;
+    }
+    // X = Z - Q M  (two's complement)
+    const uint32_t Q = static_cast<uint32_t>((qs + 0x80000000ull) >> 32);
+    uint32_t x[kLimbs];
+    uint64_t qc = 0;
+    uint32_t borrow = 0;
+#pragma unroll
+    for (int l = 0; l < kLimbs; ++l) {
+      const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
+      qc = qm >> 32;
+      const uint64_t d = static_cast<uint64_t>(z[l]) - static_cast<uint32_t>(qm) - borrow;
+      x[l] = static_cast<uint32_t>(d);
+      borrow = static_cast<uint32_t>(d >> 63);
+    }
+    bool neg = (x[kLimbs - 1] >> 31) != 0;
+    if (neg) {  // magnitude
+      uint32_t cy = 1;
+#pragma unroll
+      for (int l = 0; l < kLimbs; ++l) {
+        const uint64_t v = static_cast<uint64_t>(~x[l]) + cy;
+        x[l] = static_cast<uint32_t>(v);
+        cy = static_cast<uint32_t>(v >> 32);
+      }
+    }
+    // one correction: if |X| > M/2 the representative is M - |X| with the other sign
+    bool gt = false, decided = false;
+#pragma unroll
+    for (int l = kLimbs - 1; l >= 0; --l) {
+      if (!decided && x[l] != c.halfM[l]) {
+        gt = x[l] > c.halfM[l];
+        decided = true;
+      }
+    }
+    if (gt) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int l = 0; l < kLimbs; ++l) {
+        const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
+        x[l] = static_cast<uint32_t>(d);
+        b = static_cast<uint32_t>(d >> 63);
+      }
+      neg = !neg;
+    }
+    const int D = 2 * c.kA - E - F;  // d_i + e_j
+    *out = __longlong_as_double(static_cast<long long>(round_scaled_bits(x, neg, D)));
+  }
+}
+
+cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
+                       const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
+  if (m == 0 || n == 0) return cudaSuccess;
+  dim3 grid((m + 255) / 256, n < 65535 ? n : 65535);
+  crt_kernel<<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  return cudaGetLastError();
+}
+
+}  // namespace oz

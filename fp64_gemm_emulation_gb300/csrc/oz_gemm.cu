@@ -1,0 +1,329 @@
+// oz_gemm.cu -- steps a3 + a4: one exact integer GEMM per modulus, then mod m_t.
+//
+// [Ozaki II] Algorithm 1, step 3: C'_t = A'_t B'_t exactly, C''_t = C'_t mod m_t.
+// The pages run this as an INT8 x INT8 -> INT32 GEMM.  sm_103a has no INT8 tcgen05
+// MMA, so the same exact products run on the BF16 tensor-core path: every residue in
+// [-128, 127] is exact in bf16, every product (<= 2^14) is exact, and the FP32
+// accumulator in tensor memory adds integers exactly while |partial sum| <= 2^24.
+// The k loop is therefore cut into chunks of 960 (= 15 stages of 64):
+//     255 + 960 * 2^14 < 2^24,
+// and after each chunk the epilogue warps reduce the accumulator mod m_t in place
+// (tcgen05.ld -> exact float remainder -> tcgen05.st), so the next chunk accumulates
+// on a value in [0, m_t).  Two accumulators alternate so the tensor cores keep
+// running while one is being reduced.  The last two chunks of a tile are not written
+// back: their residues are combined in the uint8 output plane (store, then add mod m).
+// This replaces the pages' block multiplication for k >= 2^17: the result is exact
+// for every k.
+//
+// Kernel shape (one CTA per SM, persistent over work units (tile, modulus)):
+//   tile 128 x 256 (UMMA M=128, N=256, K=16), stage = 64 k (128-byte rows, 128B swizzle)
+//   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer   warps 2-5: epilogue
+//   TMEM: 512 columns = two 128 x 256 FP32 accumulators.
+// Every mbarrier wait is bounded (oz::mbar_wait); on expiry the CTA records
+// OZ_ETIMEOUT in the device status word, drains what it issued and returns.
+#include <cuda.h>
+
+#include "oz_device.cuh"
+#include "oz_internal.h"
+
+namespace oz {
+
+namespace gemm {
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int KB_PER_CHUNK = 15;  // 960 k per exactly-representable chunk
+constexpr uint32_t A_STAGE = BM * BK * 2;
+constexpr uint32_t B_STAGE = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
+static_assert(255 + KB_PER_CHUNK * BK * 128 * 128 <= (1 << 24), "chunk too long for exact FP32 sums");
+}  // namespace gemm
+
+__device__ int g_status = 0;
+
+int* device_status_ptr() {
+  int* p = nullptr;
+  cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status);
+  return p;
+}
+
+__device__ __forceinline__ void record_timeout(volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicExch(&g_status, OZ_ETIMEOUT);
+}
+
+// Exact remainder of an integer-valued float v (|v| < 2^25) modulo m, in [0, m).
+__device__ __forceinline__ float exact_mod(float v, float m, float inv_m) {
+  const float q = floorf(v * inv_m);  // within 1 of floor(v/m)
+  float r = fmaf(-q, m, v);           // exact: the true value is a small integer
+  r = (r < 0.0f) ? r + m : r;
+  r = (r >= m) ? r - m : r;
+  return r;
+}
+
+struct UnitCoord {
+  int t, tm, tn;
+};
+
+__device__ __forceinline__ UnitCoord unit_coord(int u, int tiles_m, int tiles_n) {
+  // modulus outermost (all CTAs share a modulus' planes), then groups of 8 row tiles
+  // swept along the column tiles for L2 reuse of B.
+  const int per_t = tiles_m * tiles_n;
+  UnitCoord c;
+  c.t = u / per_t;
+  int r = u - c.t * per_t;
+  const int group = 8;
+  const int gsize = group * tiles_n;
+  const int g = r / gsize;
+  const int first_m = g * group;
+  const int gm = min(group, tiles_m - first_m);
+  const int in = r - g * gsize;
+  c.tm = first_m + in % gm;
+  c.tn = in / gm;
+  return c;
+}
+
+__global__ void __launch_bounds__(gemm::THREADS, 1)
+    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmConsts c, uint8_t* __restrict__ C_res, int mp, int np, int nkb) {
+  using namespace gemm;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                  // [STAGES]  TMA -> MMA
+  uint64_t* empty = bars + STAGES;        // [STAGES]  MMA -> TMA
+  uint64_t* accfull = bars + 2 * STAGES;  // [2]       MMA -> epilogue
+  uint64_t* accempty = accfull + 2;       // [2]       epilogue -> MMA
+  uint64_t* drain = accempty + 2;         // [1]       MMA drain on the error path
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = mp / BM, tiles_n = np / BN;
+  const int units = tiles_m * tiles_n * c.s;
+  const int nchunks = (nkb + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+        const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            record_timeout(abort_flag);
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_3d(sA + stage * A_STAGE, &tmA, &full[stage], kb * BK, uc.tm * BM, uc.t);
+          tma_load_3d(sB + stage * B_STAGE, &tmB, &full[stage], kb * BK, uc.tn * BN, uc.t);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Every issued copy must land before the CTA may exit: wait for the last
+      // (up to STAGES) of them.  On the normal path these completed long ago.
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (--stage < 0) {
+          stage = STAGES - 1;
+          phase ^= 1;
+        }
+        if (!mbar_wait(&full[stage], phase)) record_timeout(abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t g = 0;  // chunk counter: accumulator g & 1
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok && !*abort_flag; u += gridDim.x) {
+        for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
+          const uint32_t acc = g & 1;
+          if (!mbar_wait(&accempty[acc], ((g >> 1) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          const int kb0 = ch * KB_PER_CHUNK;
+          const int kb1 = min(nkb, kb0 + KB_PER_CHUNK);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * A_STAGE);
+            const uint32_t b_addr = smem_u32(sB + stage * B_STAGE);
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              const uint64_t ad = umma_desc_k128(a_addr + kk * UMMA_K * 2);
+              const uint64_t bd = umma_desc_k128(b_addr + kk * UMMA_K * 2);
+              const uint32_t accumulate = (ch >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
+              umma_bf16(d_tmem, ad, bd, IDESC, accumulate);
+            }
+            umma_commit(&empty[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&accfull[acc]);
+        }
+      }
+      if (!ok) record_timeout(abort_flag);
+      // Make sure no MMA is still writing tensor memory before it is released.
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0)) record_timeout(abort_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-5)
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int row_in_tile = quad * 32 + lane;
+    const long long plane = static_cast<long long>(np) * mp;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+      const float mf = c.modf[uc.t], inv = c.invf[uc.t];
+      const uint32_t mi = static_cast<uint32_t>(mf);
+      uint8_t* out = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM + row_in_tile;
+      for (int ch = 0; ch < nchunks; ++ch, ++g) {
+        const uint32_t acc = g & 1;
+        if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+          ok = false;
+          if (lane == 0) record_timeout(abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+        const bool final_chunk = (ch + 2 >= nchunks);
+        const bool first_final = final_chunk && (ch == 0 || ch == nchunks - 2);
+#pragma unroll 1
+        for (int cb = 0; cb < BN / 32; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(taddr + cb * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
+          if (!final_chunk) {
+            tmem_st32(taddr + cb * 32, v);
+          } else {
+            uint8_t* o = out + static_cast<long long>(cb * 32) * mp;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              uint32_t r = static_cast<uint32_t>(__uint_as_float(v[i]));
+              if (!first_final) {
+                r += o[static_cast<long long>(i) * mp];
+                if (r >= mi) r -= mi;
+              }
+              o[static_cast<long long>(i) * mp] = static_cast<uint8_t>(r);
+            }
+          }
+        }
+        if (!final_chunk) tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&accempty[acc]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, gemm::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled get_encode_fn() {
+  static PFN_encodeTiled fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_encodeTiled>(p);
+  }
+  return fn;
+}
+
+// 3-D map over planes [s][rows][kp] of bf16, box {64, box_rows, 1}, 128-byte swizzle.
+static bool make_plane_map(CUtensorMap* map, const void* base, int s, int rows, int kp, int box_rows) {
+  PFN_encodeTiled enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kp), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(s)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kp) * 2, static_cast<cuuint64_t>(kp) * 2 * rows};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(gemm::BK), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
+                        const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream) {
+  using namespace gemm;
+  if (mp % BM || np % BN || kp % BK) return OZ_EINVAL;
+  CUtensorMap tmA, tmB;
+  if (!make_plane_map(&tmA, A_planes, c.s, mp, kp, BM)) return OZ_ECUDA;
+  if (!make_plane_map(&tmB, B_planes, c.s, np, kp, BN)) return OZ_ECUDA;
+  if (cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+    return OZ_ECUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OZ_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OZ_ECUDA;
+  const long long units = static_cast<long long>(mp / BM) * (np / BN) * c.s;
+  const int grid = static_cast<int>(units < sms ? units : sms);
+  residue_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, c, C_res, mp, np, kp / BK);
+  return cudaGetLastError() == cudaSuccess ? OZ_OK : OZ_ECUDA;
+}
+
+}  // namespace oz

@@ -1,0 +1,67 @@
+// oz_internal.h -- declarations shared by the host orchestration and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ozaki.h"
+
+namespace oz {
+
+constexpr int kMaxModuli = OZ_MAX_MODULI;
+constexpr int kLimbs = 6;        // 32-bit limbs for CRT values (M < 2^160 for 20 moduli)
+constexpr int kPadM = 256;       // plane row padding (A rows, C_res rows)
+constexpr int kPadN = 256;       // plane row padding (B columns, C_res columns)
+constexpr int kPadK = 64;        // plane K padding (one 128-byte bf16 row of a stage)
+
+inline int64_t roundup(int64_t x, int64_t r) { return (x + r - 1) / r * r; }
+
+// Per-modulus constants for the residue split (a2).
+struct SplitConsts {
+  int s;
+  int kA;                       // k_A = k_B
+  int mod[kMaxModuli];
+  uint32_t c16[kMaxModuli];     // 2^16 mod m
+  uint32_t c32[kMaxModuli];     // 2^32 mod m
+  uint32_t magic[kMaxModuli];   // ceil(2^39 / m): y mod m for y < 2^30
+};
+
+// Constants of the CRT reconstruction (a5, a6).
+struct CrtConsts {
+  int s;
+  int kA;
+  int mod[kMaxModuli];
+  uint32_t P[kMaxModuli][kLimbs];  // M_t * y_t (< M), little-endian limbs
+  uint32_t frac[kMaxModuli];       // floor(2^32 * y_t / m_t): P_t / M in 0.32 fixed point
+  uint32_t M[kLimbs];
+  uint32_t halfM[kLimbs];          // floor(M / 2)
+};
+
+// Per-modulus constants of the GEMM epilogue (a4).
+struct GemmConsts {
+  int s;
+  float modf[kMaxModuli];
+  float invf[kMaxModuli];
+};
+
+// Host-side helpers (ozaki_host.cu).
+int fill_split_consts(int s, long long k_inner, SplitConsts* out);
+int fill_crt_consts(int s, long long k_inner, CrtConsts* out);
+
+// Kernel launchers; each returns a cudaError_t from the launch.
+cudaError_t launch_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                             int32_t* rowexp, int32_t* colexp, cudaStream_t stream);
+cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,
+                         const int32_t* exps, const SplitConsts& c, uint16_t* planes, int rows_padded,
+                         int kp, cudaStream_t stream);
+int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
+                        const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
+cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
+                       const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream);
+cudaError_t launch_fill_zero(int m, int n, double* C, int ldc, cudaStream_t stream);
+
+// Device status word (set by kernels whose bounded waits expired).
+int* device_status_ptr();
+
+}  // namespace oz

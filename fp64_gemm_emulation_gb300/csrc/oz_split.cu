@@ -1,0 +1,154 @@
+// oz_split.cu -- step a2: scale, truncate and take the symmetric residues.
+//
+// [Ozaki II] Algorithm 1, step 2 (A' = trunc(DA)) and the left half of step 3
+// (A'_t = A' mod m_t, symmetric, signed 8-bit) for every modulus t, in one pass over
+// the FP64 operand.  Integer bit manipulation only (the FP64 units are not used):
+// a' = trunc(|a| 2^d) is kept as u * 2^p with u < 2^53, and a' mod m is
+// (u mod m)(2^p mod m) mod m with u split into 16-bit limbs.
+//
+// One block handles a 64 x 64 tile (rows x k).  Phase 1 reads the tile with
+// coalesced loads along whichever index is contiguous in memory and stores the
+// packed (sign, p, u) words in shared memory; phase 2 reads them along k and writes
+// 16-byte vectors of 8 bf16 residues per modulus, so the K-contiguous planes are
+// written in full 128-byte rows.
+#include "oz_internal.h"
+
+namespace oz {
+
+constexpr int kSplitTile = 64;
+constexpr int kSplitThreads = 256;
+
+// Packs trunc(|x| 2^(kA - E)) as sign<<63 | p<<53 | u, value u 2^p (u < 2^53).
+__device__ __forceinline__ uint64_t pack_scaled(double x, int E, int kA) {
+  if (E == OZ_EXP_EMPTY || E == OZ_EXP_NONFINITE) return 0;
+  const uint64_t bits = static_cast<uint64_t>(__double_as_longlong(x));
+  const int ex = static_cast<int>((bits >> 52) & 0x7FF);
+  if (ex == 0x7FF) return 0;
+  const uint64_t frac = bits & 0x000FFFFFFFFFFFFFull;
+  uint64_t mant;
+  int e2;
+  if (ex == 0) {
+    mant = frac;
+    e2 = -1074;
+  } else {
+    mant = frac | (1ull << 52);
+    e2 = ex - 1075;
+  }
+  const int sh = e2 + (kA - E);  // |x| 2^d = mant 2^sh
+  uint64_t u;
+  uint32_t p;
+  if (sh >= 0) {
+    u = mant;
+    p = static_cast<uint32_t>(sh);
+  } else {
+    u = (-sh >= 64) ? 0 : (mant >> (-sh));  // truncation toward zero
+    p = 0;
+  }
+  if (u == 0) return 0;
+  return (bits & 0x8000000000000000ull) | (static_cast<uint64_t>(p) << 53) | u;
+}
+
+// y mod m for y < 2^30 and 2 <= m <= 256, with magic = ceil(2^39 / m).
+__device__ __forceinline__ uint32_t mod_small(uint32_t y, uint32_t m, uint32_t magic) {
+  return y - (__umulhi(y, magic) >> 7) * m;
+}
+
+// Symmetric residue of the packed integer modulo m, in [-(m/2), (m-1)/2].
+__device__ __forceinline__ int sym_residue(uint64_t packed, uint32_t m, uint32_t c16, uint32_t c32,
+                                           uint32_t magic) {
+  const uint64_t u = packed & ((1ull << 53) - 1);
+  const uint32_t p = static_cast<uint32_t>(packed >> 53) & 0x3FFu;
+  const uint32_t x0 = static_cast<uint32_t>(u) & 0xFFFFu;
+  const uint32_t x1 = static_cast<uint32_t>(u) >> 16;
+  const uint32_t x2 = static_cast<uint32_t>(u >> 32);
+  uint32_t r = mod_small(x2 * c32 + x1 * c16 + x0, m, magic);
+  if (p != 0) {
+    uint32_t w = 1;
+    for (uint32_t i = 0; i < p && w != 0; ++i) {
+      w <<= 1;
+      if (w >= m) w -= m;
+    }
+    r = mod_small(r * w, m, magic);
+  }
+  const int h = static_cast<int>((m + 1) >> 1);
+  int v = static_cast<int>(r);
+  if (v >= h) v -= static_cast<int>(m);
+  if (packed >> 63) {
+    v = -v;
+    if (v >= h) v -= static_cast<int>(m);
+  }
+  return v;
+}
+
+// bf16 bit pattern of a small integer (|v| <= 256 is exact in bf16).
+__device__ __forceinline__ uint32_t bf16_bits(int v) {
+  return __float_as_uint(static_cast<float>(v)) >> 16;
+}
+
+template <bool kRowsContiguous>
+__global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, const double* __restrict__ X,
+                                                              long long rs, long long ks,
+                                                              const int32_t* __restrict__ exps,
+                                                              const SplitConsts c, uint16_t* __restrict__ planes,
+                                                              int rows_padded, int kp) {
+  __shared__ uint64_t tile[kSplitTile][kSplitTile + 1];  // [kk][r]
+  const int tid = threadIdx.x;
+  const int k0 = blockIdx.x * kSplitTile;
+  const int r0 = blockIdx.y * kSplitTile;
+
+#pragma unroll 4
+  for (int it = 0; it < (kSplitTile * kSplitTile) / kSplitThreads; ++it) {
+    int r, kk;
+    if (kRowsContiguous) {
+      r = tid & 63;
+      kk = (tid >> 6) + 4 * it;
+    } else {
+      kk = tid & 63;
+      r = (tid >> 6) + 4 * it;
+    }
+    const int gr = r0 + r, gk = k0 + kk;
+    uint64_t packed = 0;
+    if (gr < rows && gk < K) packed = pack_scaled(__ldg(X + gr * rs + gk * ks), __ldg(exps + gr), c.kA);
+    tile[kk][r] = packed;
+  }
+  __syncthreads();
+
+  const long long plane_elems = static_cast<long long>(rows_padded) * kp;
+#pragma unroll 1
+  for (int it = 0; it < (kSplitTile * kSplitTile / 8) / kSplitThreads; ++it) {
+    const int item = tid + kSplitThreads * it;
+    const int g = item & 7;   // group of 8 consecutive k
+    const int r = item >> 3;  // row within the tile
+    uint64_t v[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v[x] = tile[g * 8 + x][r];
+    uint16_t* dst = planes + static_cast<long long>(r0 + r) * kp + k0 + g * 8;
+#pragma unroll 1
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
+      uint32_t w[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t lo = bf16_bits(sym_residue(v[2 * x], m, c16, c32, mg));
+        const uint32_t hi = bf16_bits(sym_residue(v[2 * x + 1], m, c16, c32, mg));
+        w[x] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,
+                         const int32_t* exps, const SplitConsts& c, uint16_t* planes, int rows_padded, int kp,
+                         cudaStream_t stream) {
+  dim3 grid(kp / kSplitTile, rows_padded / kSplitTile);
+  if (row_stride == 1)
+    split_kernel<true><<<grid, kSplitThreads, 0, stream>>>(rows, k, X, row_stride, k_stride, exps, c, planes,
+                                                           rows_padded, kp);
+  else
+    split_kernel<false><<<grid, kSplitThreads, 0, stream>>>(rows, k, X, row_stride, k_stride, exps, c, planes,
+                                                            rows_padded, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace oz

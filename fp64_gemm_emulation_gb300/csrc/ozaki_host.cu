@@ -1,0 +1,447 @@
+// ozaki_host.cu -- the C ABI of libozaki: argument checks, parameters, workspace,
+// and the launch sequence of the Ozaki Scheme II path.
+//
+// Parameters follow [Ozaki II]: the moduli (section 6: 2 <= m_t <= 256, pairwise
+// coprime; the greedy descending list from 256 is used), M = prod m_t, M_t = M / m_t,
+// y_t = M_t^{-1} mod m_t (section 4), and k_A = k_B = the largest k with
+// q 2^(2k) <= M/2 - 1 (section 5), computed exactly on multi-limb integers.
+#include <cstdio>
+#include <cstring>
+
+#include "oz_internal.h"
+
+namespace oz {
+namespace {
+
+// ---------------------------------------------------------------- small big-integer
+constexpr int kBigLimbs = 8;  // 256 bits: M < 2^160, q 4^k < 2^162
+struct Big {
+  uint32_t w[kBigLimbs];
+};
+
+Big big_from(uint64_t v) {
+  Big b{};
+  b.w[0] = static_cast<uint32_t>(v);
+  b.w[1] = static_cast<uint32_t>(v >> 32);
+  return b;
+}
+
+Big big_mul_small(const Big& a, uint32_t m) {
+  Big r{};
+  uint64_t carry = 0;
+  for (int i = 0; i < kBigLimbs; ++i) {
+    const uint64_t v = static_cast<uint64_t>(a.w[i]) * m + carry;
+    r.w[i] = static_cast<uint32_t>(v);
+    carry = v >> 32;
+  }
+  return r;
+}
+
+Big big_div_small(const Big& a, uint32_t m, uint32_t* rem) {
+  Big q{};
+  uint64_t r = 0;
+  for (int i = kBigLimbs - 1; i >= 0; --i) {
+    const uint64_t cur = (r << 32) | a.w[i];
+    q.w[i] = static_cast<uint32_t>(cur / m);
+    r = cur % m;
+  }
+  if (rem) *rem = static_cast<uint32_t>(r);
+  return q;
+}
+
+int big_cmp(const Big& a, const Big& b) {
+  for (int i = kBigLimbs - 1; i >= 0; --i)
+    if (a.w[i] != b.w[i]) return a.w[i] < b.w[i] ? -1 : 1;
+  return 0;
+}
+
+Big big_sub_small(const Big& a, uint32_t v) {
+  Big r = a;
+  uint64_t borrow = v;
+  for (int i = 0; i < kBigLimbs && borrow; ++i) {
+    const uint64_t cur = r.w[i];
+    r.w[i] = static_cast<uint32_t>(cur - borrow);
+    borrow = cur < borrow ? 1 : 0;
+  }
+  return r;
+}
+
+// The greedy descending pairwise-coprime list starting at 256.
+int greedy_moduli(int s, int* out) {
+  int count = 0;
+  for (int cand = 256; cand >= 2 && count < s; --cand) {
+    bool ok = true;
+    for (int i = 0; i < count && ok; ++i) {
+      int a = cand, b = out[i];
+      while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+      }
+      ok = (a == 1);
+    }
+    if (ok) out[count++] = cand;
+  }
+  return count;
+}
+
+struct Params {
+  int s;
+  int mod[kMaxModuli];
+  Big M;
+  Big P[kMaxModuli];  // M_t * y_t
+  int y[kMaxModuli];
+};
+
+int make_params(int s, Params* p) {
+  if (s < 1 || s > kMaxModuli) return OZ_EINVAL;
+  p->s = s;
+  if (greedy_moduli(s, p->mod) != s) return OZ_EINVAL;
+  p->M = big_from(1);
+  for (int t = 0; t < s; ++t) p->M = big_mul_small(p->M, static_cast<uint32_t>(p->mod[t]));
+  for (int t = 0; t < s; ++t) {
+    const uint32_t m = static_cast<uint32_t>(p->mod[t]);
+    uint32_t unused;
+    const Big Mt = big_div_small(p->M, m, &unused);
+    uint32_t Mt_mod;
+    big_div_small(Mt, m, &Mt_mod);
+    int y = -1;
+    for (uint32_t c = 1; c < m; ++c)
+      if ((static_cast<uint64_t>(Mt_mod) * c) % m == 1) {
+        y = static_cast<int>(c);
+        break;
+      }
+    if (y < 0) return OZ_EINVAL;
+    p->y[t] = y;
+    p->P[t] = big_mul_small(Mt, static_cast<uint32_t>(y));
+  }
+  return OZ_OK;
+}
+
+// Largest k >= 0 with 2 q 4^k <= M - 2; -1 if none.
+int choose_k(const Big& M, long long q) {
+  if (q < 1) return -1;
+  const Big lim = big_sub_small(M, 2);
+  Big t = big_mul_small(big_from(static_cast<uint64_t>(q)), 2);
+  if (big_cmp(t, lim) > 0) return -1;
+  int k = 0;
+  while (true) {
+    const Big t4 = big_mul_small(t, 4);
+    if (big_cmp(t4, lim) > 0) break;
+    t = t4;
+    ++k;
+  }
+  return k;
+}
+
+}  // namespace
+
+int fill_split_consts(int s, long long k_inner, SplitConsts* out) {
+  Params p;
+  int rc = make_params(s, &p);
+  if (rc) return rc;
+  const int k = choose_k(p.M, k_inner);
+  if (k < 1) return OZ_ERANGE;
+  std::memset(out, 0, sizeof(*out));
+  out->s = s;
+  out->kA = k;
+  for (int t = 0; t < s; ++t) {
+    const uint32_t m = static_cast<uint32_t>(p.mod[t]);
+    out->mod[t] = p.mod[t];
+    out->c16[t] = (1u << 16) % m;
+    out->c32[t] = static_cast<uint32_t>((1ull << 32) % m);
+    out->magic[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
+  }
+  return OZ_OK;
+}
+
+int fill_crt_consts(int s, long long k_inner, CrtConsts* out) {
+  Params p;
+  int rc = make_params(s, &p);
+  if (rc) return rc;
+  const int k = choose_k(p.M, k_inner);
+  if (k < 1) return OZ_ERANGE;
+  std::memset(out, 0, sizeof(*out));
+  out->s = s;
+  out->kA = k;
+  for (int l = kLimbs; l < kBigLimbs; ++l)
+    if (p.M.w[l]) return OZ_EINVAL;  // cannot happen for <= 20 moduli <= 256
+  uint32_t unused;
+  const Big half = big_div_small(p.M, 2, &unused);
+  for (int l = 0; l < kLimbs; ++l) {
+    out->M[l] = p.M.w[l];
+    out->halfM[l] = half.w[l];
+  }
+  for (int t = 0; t < s; ++t) {
+    out->mod[t] = p.mod[t];
+    for (int l = 0; l < kLimbs; ++l) out->P[t][l] = p.P[t].w[l];
+    out->frac[t] = static_cast<uint32_t>((static_cast<uint64_t>(p.y[t]) << 32) / static_cast<uint64_t>(p.mod[t]));
+  }
+  return OZ_OK;
+}
+
+}  // namespace oz
+
+using namespace oz;
+
+namespace {
+
+struct Layout {
+  int mp, np, kp;
+  size_t off_rowexp, off_colexp, off_A, off_B, off_C, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout make_layout(int m, int n, int k, int s) {
+  Layout L;
+  L.mp = static_cast<int>(roundup(m, kPadM));
+  L.np = static_cast<int>(roundup(n, kPadN));
+  L.kp = static_cast<int>(roundup(k, kPadK));
+  size_t off = 0;
+  L.off_rowexp = off;
+  off = align256(off + sizeof(int32_t) * static_cast<size_t>(m));
+  L.off_colexp = off;
+  off = align256(off + sizeof(int32_t) * static_cast<size_t>(n));
+  L.off_A = off;
+  off = align256(off + sizeof(uint16_t) * static_cast<size_t>(s) * L.mp * L.kp);
+  L.off_B = off;
+  off = align256(off + sizeof(uint16_t) * static_cast<size_t>(s) * L.np * L.kp);
+  L.off_C = off;
+  off = align256(off + static_cast<size_t>(s) * L.np * L.mp);
+  L.total = off;
+  return L;
+}
+
+int check_dims(int m, int n, int k, int lda, int ldb, int ldc) {
+  if (m < 0 || n < 0 || k < 0) return OZ_EINVAL;
+  if (lda < (m > 1 ? m : 1) || ldb < (k > 1 ? k : 1) || ldc < (m > 1 ? m : 1)) return OZ_EINVAL;
+  return OZ_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? OZ_OK : OZ_ECUDA; }
+
+// The allocating entry points draw their workspace from the device's default
+// stream-ordered memory pool.  Raise its release threshold once per device so the
+// pool keeps the memory between calls instead of unmapping it at every
+// synchronisation (repeated calls then allocate in microseconds).
+void keep_default_pool_cached() {
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || done[dev]) return;
+  cudaMemPool_t pool;
+  if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+    uint64_t threshold = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+  }
+  cudaGetLastError();
+  done[dev] = true;
+}
+
+GemmConsts make_gemm_consts(const SplitConsts& sc) {
+  GemmConsts g{};
+  g.s = sc.s;
+  for (int t = 0; t < sc.s; ++t) {
+    g.modf[t] = static_cast<float>(sc.mod[t]);
+    g.invf[t] = static_cast<float>(1.0 / sc.mod[t]);
+  }
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ozaki2_moduli(int num_moduli, int* moduli_out) {
+  if (!moduli_out || num_moduli < 1 || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  return oz::greedy_moduli(num_moduli, moduli_out) == num_moduli ? OZ_OK : OZ_EINVAL;
+}
+
+int ozaki2_choose_k(int num_moduli, long long k_inner, int* k_out) {
+  if (!k_out || k_inner < 1) return OZ_EINVAL;
+  Params p;
+  const int rc = make_params(num_moduli, &p);
+  if (rc) return rc;
+  const int k = oz::choose_k(p.M, k_inner);
+  if (k < 1) return OZ_ERANGE;
+  *k_out = k;
+  return OZ_OK;
+}
+
+int ozaki2_plane_dims(int m, int n, int k, int* mp, int* np, int* kp) {
+  if (m < 0 || n < 0 || k < 0 || !mp || !np || !kp) return OZ_EINVAL;
+  *mp = static_cast<int>(roundup(m, kPadM));
+  *np = static_cast<int>(roundup(n, kPadN));
+  *kp = static_cast<int>(roundup(k, kPadK));
+  return OZ_OK;
+}
+
+size_t ozaki2_workspace_bytes(int m, int n, int k, int num_moduli) {
+  if (m < 0 || n < 0 || k < 0 || num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return 0;
+  return make_layout(m, n, k, num_moduli).total;
+}
+
+int ozaki2_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int32_t* rowexp,
+                     int32_t* colexp, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0) return OZ_EINVAL;
+  if ((A && (lda < (m > 1 ? m : 1) || !rowexp)) || (B && (ldb < (k > 1 ? k : 1) || !colexp))) return OZ_EINVAL;
+  return cuda_rc(launch_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream));
+}
+
+int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
+                 const int32_t* rowexp, const int32_t* colexp, uint16_t* A_planes, uint16_t* B_planes,
+                 cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1) return OZ_EINVAL;
+  if ((A && (lda < (m > 1 ? m : 1) || !rowexp || !A_planes)) || (B && (ldb < (k > 1 ? k : 1) || !colexp || !B_planes)))
+    return OZ_EINVAL;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  SplitConsts sc;
+  int rc = fill_split_consts(num_moduli, k, &sc);
+  if (rc) return rc;
+  const int mp = static_cast<int>(roundup(m, kPadM)), np = static_cast<int>(roundup(n, kPadN)),
+            kp = static_cast<int>(roundup(k, kPadK));
+  if (A && m > 0) {
+    rc = cuda_rc(launch_split(m, k, A, 1, lda, rowexp, sc, A_planes, mp, kp, stream));
+    if (rc) return rc;
+  }
+  if (B && n > 0) {
+    rc = cuda_rc(launch_split(n, k, B, ldb, 1, colexp, sc, B_planes, np, kp, stream));
+    if (rc) return rc;
+  }
+  return OZ_OK;
+}
+
+int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_planes, const uint16_t* B_planes,
+                        uint8_t* C_res, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || !A_planes || !B_planes || !C_res) return OZ_EINVAL;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  SplitConsts sc;
+  const int rc = fill_split_consts(num_moduli, k, &sc);
+  if (rc) return rc;
+  return launch_residue_gemm(static_cast<int>(roundup(m, kPadM)), static_cast<int>(roundup(n, kPadN)),
+                             static_cast<int>(roundup(k, kPadK)), make_gemm_consts(sc), A_planes, B_planes, C_res,
+                             stream);
+}
+
+int ozaki2_crt(int m, int n, int k, int num_moduli, const uint8_t* C_res, const int32_t* rowexp,
+               const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || !C_res || !rowexp || !colexp || !C || ldc < (m > 1 ? m : 1)) return OZ_EINVAL;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  CrtConsts cc;
+  const int rc = fill_crt_consts(num_moduli, k, &cc);
+  if (rc) return rc;
+  return cuda_rc(launch_crt(m, n, static_cast<int>(roundup(m, kPadM)), static_cast<int>(roundup(n, kPadN)), cc,
+                            C_res, rowexp, colexp, C, ldc, stream));
+}
+
+int ozaki2_dgemm_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                    int num_moduli, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_dims(m, n, k, lda, ldb, ldc);
+  if (rc) return rc;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (!C) return OZ_EINVAL;
+  if (k == 0) return cuda_rc(launch_fill_zero(m, n, C, ldc, stream));
+  if (!A || !B) return OZ_EINVAL;
+  {
+    int kA;
+    rc = ozaki2_choose_k(num_moduli, k, &kA);
+    if (rc) return rc;
+  }
+  const Layout L = make_layout(m, n, k, num_moduli);
+  if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) return OZ_ENOMEM;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* rowexp = reinterpret_cast<int32_t*>(ws + L.off_rowexp);
+  int32_t* colexp = reinterpret_cast<int32_t*>(ws + L.off_colexp);
+  uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + L.off_A);
+  uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + L.off_B);
+  uint8_t* Cr = ws + L.off_C;
+  if ((rc = ozaki2_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream))) return rc;
+  if ((rc = ozaki2_split(m, n, k, A, lda, B, ldb, num_moduli, rowexp, colexp, Ap, Bp, stream))) return rc;
+  if ((rc = ozaki2_residue_gemm(m, n, k, num_moduli, Ap, Bp, Cr, stream))) return rc;
+  return ozaki2_crt(m, n, k, num_moduli, Cr, rowexp, colexp, C, ldc, stream);
+}
+
+int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                 int num_moduli, cudaStream_t stream) {
+  int rc = check_dims(m, n, k, lda, ldb, ldc);
+  if (rc) return rc;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (k == 0) return C ? cuda_rc(launch_fill_zero(m, n, C, ldc, stream)) : OZ_EINVAL;
+  const size_t bytes = ozaki2_workspace_bytes(m, n, k, num_moduli);
+  keep_default_pool_cached();
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return OZ_ENOMEM;
+  }
+  rc = ozaki2_dgemm_ws(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, ws, bytes, stream);
+  const cudaError_t e = cudaFreeAsync(ws, stream);
+  if (rc == OZ_OK && e != cudaSuccess) rc = OZ_ECUDA;
+  return rc;
+}
+
+int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                      int num_moduli) {
+  int rc = check_dims(m, n, k, lda, ldb, ldc);
+  if (rc) return rc;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (!C || (k > 0 && (!A || !B))) return OZ_EINVAL;
+  cudaStream_t st;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return OZ_ECUDA;
+  keep_default_pool_cached();
+  const size_t a_bytes = sizeof(double) * static_cast<size_t>(lda) * (k > 0 ? k : 1);
+  const size_t b_bytes = sizeof(double) * static_cast<size_t>(ldb) * n;
+  const size_t c_bytes = sizeof(double) * static_cast<size_t>(ldc) * n;
+  double *dA = nullptr, *dB = nullptr, *dC = nullptr;
+  rc = OZ_OK;
+  if (cudaMallocAsync(&dA, a_bytes, st) != cudaSuccess || cudaMallocAsync(&dB, b_bytes, st) != cudaSuccess ||
+      cudaMallocAsync(&dC, c_bytes, st) != cudaSuccess)
+    rc = OZ_ENOMEM;
+  if (!rc && k > 0) {
+    if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+      rc = OZ_ECUDA;
+  }
+  if (!rc && ldc != m) {  // keep the caller's padding rows of C intact
+    if (cudaMemcpyAsync(dC, C, c_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) rc = OZ_ECUDA;
+  }
+  if (!rc) rc = ozaki2_dgemm(m, n, k, dA, lda, dB, ldb, dC, ldc, num_moduli, st);
+  if (!rc && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) rc = OZ_ECUDA;
+  if (dA) cudaFreeAsync(dA, st);
+  if (dB) cudaFreeAsync(dB, st);
+  if (dC) cudaFreeAsync(dC, st);
+  if (cudaStreamSynchronize(st) != cudaSuccess && !rc) rc = OZ_ECUDA;
+  cudaStreamDestroy(st);
+  cudaGetLastError();
+  return rc;
+}
+
+int ozaki_get_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return OZ_ECUDA;
+  int* p = device_status_ptr();
+  if (!p) return OZ_ECUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return OZ_ECUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return OZ_ECUDA;
+  return v;
+}
+
+const char* ozaki_status_string(int status) {
+  switch (status) {
+    case OZ_OK: return "OZ_OK";
+    case OZ_EINVAL: return "OZ_EINVAL: invalid argument";
+    case OZ_ERANGE: return "OZ_ERANGE: too few moduli for this inner dimension";
+    case OZ_ECUDA: return "OZ_ECUDA: CUDA runtime error";
+    case OZ_ENOMEM: return "OZ_ENOMEM: workspace allocation failed or too small";
+    case OZ_ETIMEOUT: return "OZ_ETIMEOUT: a bounded device wait expired";
+    case OZ_ENODEV: return "OZ_ENODEV: no usable device";
+    default: return "unknown ozaki status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,231 @@
+"""Python binding of libozaki (argument marshalling only; every step runs in the CUDA kernels).
+
+The functions carry the C ABI's names (``include/ozaki.h``).  Device operands are
+torch CUDA tensors; matrices are column-major float64 (a tensor ``X`` of shape
+(rows, cols) with ``X.stride(0) == 1``; :func:`colmajor` makes one).  Calls are
+ordered on the current torch CUDA stream unless ``stream`` is given.
+
+There is no fallback: if ``libozaki.so`` is missing or fails to load, importing
+this module raises, and every call reports the library's status code as an
+exception.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libozaki.so")
+
+OZ_OK, OZ_EINVAL, OZ_ERANGE, OZ_ECUDA, OZ_ENOMEM, OZ_ETIMEOUT, OZ_ENODEV = 0, -1, -2, -3, -4, -5, -6
+OZ_EXP_EMPTY = np.int32(np.uint32(0x80808080).view(np.int32))
+OZ_EXP_NONFINITE = np.int32(0x7FFFFFFF)
+PAD_M, PAD_N, PAD_K = 256, 256, 64
+
+
+class OzakiError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {_lib.ozaki_status_string(code).decode()}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m fp64_gemm_emulation_gb300.build_lib`")
+    lib = ctypes.CDLL(LIB_PATH)
+    I, L, P, S = ctypes.c_int, ctypes.c_longlong, ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "ozaki2_moduli": (I, [I, P]),
+        "ozaki2_choose_k": (I, [I, L, P]),
+        "ozaki2_plane_dims": (I, [I, I, I, P, P, P]),
+        "ozaki2_workspace_bytes": (S, [I, I, I, I]),
+        "ozaki2_exponents": (I, [I, I, I, P, I, P, I, P, P, P]),
+        "ozaki2_split": (I, [I, I, I, P, I, P, I, I, P, P, P, P, P]),
+        "ozaki2_residue_gemm": (I, [I, I, I, I, P, P, P, P]),
+        "ozaki2_crt": (I, [I, I, I, I, P, P, P, P, I, P]),
+        "ozaki2_dgemm_ws": (I, [I, I, I, P, I, P, I, P, I, I, P, S, P]),
+        "ozaki2_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
+        "ozaki2_dgemm_host": (I, [I, I, I, P, I, P, I, P, I, I]),
+        "ozaki_get_device_status": (I, []),
+        "ozaki_status_string": (ctypes.c_char_p, [I]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OZ_OK:
+        raise OzakiError(rc, where)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def colmajor(x):
+    """A column-major copy (or view) of a 2-D tensor: same shape, stride(0) == 1."""
+    return x if (x.dim() == 2 and x.stride(0) == 1 and x.stride(1) >= max(1, x.shape[0])) else x.t().contiguous().t()
+
+
+def _ld(x) -> int:
+    assert x.dim() == 2 and x.stride(0) == 1, "operand must be column-major (stride(0) == 1)"
+    return max(1, int(x.stride(1)), int(x.shape[0]))
+
+
+# ------------------------------------------------------------------ host-only queries
+def ozaki2_moduli(num_moduli: int) -> list[int]:
+    out = (ctypes.c_int * max(1, num_moduli))()
+    _check(_lib.ozaki2_moduli(num_moduli, out), "ozaki2_moduli")
+    return list(out[:num_moduli])
+
+
+def ozaki2_choose_k(num_moduli: int, k_inner: int) -> int:
+    k = ctypes.c_int()
+    _check(_lib.ozaki2_choose_k(num_moduli, k_inner, ctypes.byref(k)), "ozaki2_choose_k")
+    return k.value
+
+
+def ozaki2_plane_dims(m: int, n: int, k: int) -> tuple[int, int, int]:
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(_lib.ozaki2_plane_dims(m, n, k, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), "ozaki2_plane_dims")
+    return a.value, b.value, c.value
+
+
+def ozaki2_workspace_bytes(m: int, n: int, k: int, num_moduli: int) -> int:
+    return int(_lib.ozaki2_workspace_bytes(m, n, k, num_moduli))
+
+
+# ------------------------------------------------------------------ steps
+def ozaki2_exponents(A, B, stream=None):
+    """Step a1: (rowexp[m], colexp[n]) int32 tensors on A's device."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    rowexp = torch.empty(m, dtype=torch.int32, device=A.device)
+    colexp = torch.empty(n, dtype=torch.int32, device=A.device)
+    _check(_lib.ozaki2_exponents(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(rowexp), _ptr(colexp),
+                                 _stream(stream)), "ozaki2_exponents")
+    return rowexp, colexp
+
+
+def ozaki2_split(A, B, num_moduli: int, rowexp, colexp, stream=None):
+    """Step a2: bf16-bit residue planes (uint16 views as int16 tensors) [s, Mp, Kp] and [s, Np, Kp]."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    Ap = torch.empty((num_moduli, mp, kp), dtype=torch.int16, device=A.device)
+    Bp = torch.empty((num_moduli, np_, kp), dtype=torch.int16, device=A.device)
+    _check(_lib.ozaki2_split(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_moduli, _ptr(rowexp), _ptr(colexp),
+                             _ptr(Ap), _ptr(Bp), _stream(stream)), "ozaki2_split")
+    return Ap, Bp
+
+
+def ozaki2_residue_gemm(m: int, n: int, k: int, num_moduli: int, A_planes, B_planes, stream=None):
+    """Steps a3+a4: C_res uint8 tensor [s, Np, Mp] with C''_t = (A'_t B'_t) mod m_t."""
+    import torch
+
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    Cr = torch.empty((num_moduli, np_, mp), dtype=torch.uint8, device=A_planes.device)
+    _check(_lib.ozaki2_residue_gemm(m, n, k, num_moduli, _ptr(A_planes), _ptr(B_planes), _ptr(Cr),
+                                    _stream(stream)), "ozaki2_residue_gemm")
+    return Cr
+
+
+def ozaki2_crt(m: int, n: int, k: int, num_moduli: int, C_res, rowexp, colexp, C=None, stream=None):
+    """Steps a5+a6: C (m x n column-major float64)."""
+    import torch
+
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=C_res.device).t()
+    _check(_lib.ozaki2_crt(m, n, k, num_moduli, _ptr(C_res), _ptr(rowexp), _ptr(colexp), _ptr(C), _ld(C),
+                           _stream(stream)), "ozaki2_crt")
+    return C
+
+
+# ------------------------------------------------------------------ composed
+def ozaki2_dgemm(A, B, num_moduli: int = 14, C=None, stream=None):
+    """C = A B by Ozaki Scheme II (stream-ordered workspace allocation inside the library)."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    _check(_lib.ozaki2_dgemm(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli,
+                             _stream(stream)), "ozaki2_dgemm")
+    return C
+
+
+def ozaki2_dgemm_ws(A, B, num_moduli: int, workspace, C=None, stream=None):
+    """C = A B using a caller-owned device workspace (a uint8 tensor of at least
+    ozaki2_workspace_bytes(m, n, k, num_moduli) bytes)."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    _check(_lib.ozaki2_dgemm_ws(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli,
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ozaki2_dgemm_ws")
+    return C
+
+
+def ozaki2_dgemm_host(A: np.ndarray, B: np.ndarray, num_moduli: int = 14, C: np.ndarray | None = None):
+    """C = A B with HOST (numpy, column-major float64) operands; synchronous."""
+    A = np.asfortranarray(A, dtype=np.float64)
+    B = np.asfortranarray(B, dtype=np.float64)
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = np.empty((m, n), dtype=np.float64, order="F")
+    assert C.flags.f_contiguous and C.dtype == np.float64
+    _check(_lib.ozaki2_dgemm_host(m, n, k, A.ctypes.data, max(1, m), B.ctypes.data, max(1, k), C.ctypes.data,
+                                  max(1, m), num_moduli), "ozaki2_dgemm_host")
+    return C
+
+
+def ozaki2_dgemm_host_ptr(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli):
+    """Raw-pointer form of ozaki2_dgemm_host (host pointers, e.g. pinned torch tensors)."""
+    _check(_lib.ozaki2_dgemm_host(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli), "ozaki2_dgemm_host")
+
+
+def ozaki_get_device_status() -> int:
+    return int(_lib.ozaki_get_device_status())
+
+
+def ozaki_status_string(code: int) -> str:
+    return _lib.ozaki_status_string(code).decode()
+
+
+def exported_symbols() -> list[str]:
+    """Names the loaded library exports among those ``include/ozaki.h`` declares."""
+    return [name for name in _declared_names() if hasattr(_lib, name)]
+
+
+def _declared_names() -> list[str]:
+    import re
+
+    hdr = os.path.join(os.path.dirname(_PKG), "include", "ozaki.h")
+    with open(hdr) as f:
+        text = f.read()
+    return re.findall(r"^(?:int|size_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)

@@ -1,0 +1,151 @@
+/*
+ * ozaki.h -- C ABI of libozaki: FP64 matrix multiplication emulated on low-precision
+ * tensor cores with the Ozaki scheme, for NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Ozaki Scheme II: mapping high-precision GEMM to a few INT8 GEMMs with CRT"
+ * (explainer of Ozaki, Uchino, Imamura, arXiv:2504.08009), cited below as [Ozaki II];
+ * Algorithm 1 is in its section 7 (steps 1-6).  Scheme I follows the "Ozaki Scheme"
+ * course notes (SplitFP / RN split / triangular products), cited as [Ozaki notes].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Matrices are column-major with leading dimensions (BLAS / cuBLAS convention):
+ *    A is m x k (lda >= max(1,m)), B is k x n (ldb >= max(1,k)), C is m x n
+ *    (ldc >= max(1,m)).  The operation is C = A*B: no alpha/beta, no transposes,
+ *    C is overwritten.
+ *  - Unless a name ends in _host, every pointer is DEVICE memory owned by the caller;
+ *    the library never frees it.  Calls are asynchronous and ordered on `stream`
+ *    (0 = legacy default stream); nothing synchronises the device implicitly.
+ *  - Return value: OZ_OK (0) or a negative oz_status.  Argument errors are reported
+ *    synchronously before anything is launched.  A device-side failure (a bounded wait
+ *    inside a kernel that expired) is recorded in a device status word that
+ *    ozaki_get_device_status() returns.
+ *  - m, n or k equal to 0: nothing is read; for k = 0 (m, n > 0) C is set to +0.0.
+ *  - Inputs holding Inf or NaN: the affected rows of C (row of A) and columns of C
+ *    (column of B) are set to NaN; nothing traps.
+ *
+ * Scheme II workspace layout (what the step entry points read and write)
+ * ----------------------------------------------------------------------
+ *  Let Mp = roundup(m, 256), Np = roundup(n, 256), Kp = roundup(k, 64), s = num_moduli.
+ *  - rowexp[m], colexp[n] (int32): E_i = ceil(log2 max_j |a_ij|) and
+ *    F_j = ceil(log2 max_l |b_lj|); OZ_EXP_EMPTY for an all-zero row/column,
+ *    OZ_EXP_NONFINITE when it holds Inf/NaN.
+ *  - A_planes [s][Mp][Kp] and B_planes [s][Np][Kp]: bf16 bit patterns (uint16) holding
+ *    the symmetric residues A'_t = A' mod m_t and B'_t = B' mod m_t, integers in
+ *    [-128, 127] that bf16 represents exactly.  Row i of A_planes[t] is row i of A'_t
+ *    (K contiguous); row j of B_planes[t] is column j of B'_t (K contiguous).  Padding
+ *    rows / columns are zero.
+ *  - C_res [s][Np][Mp] (uint8): C''_t = (A'_t B'_t) mod m_t in [0, m_t), column-major
+ *    per modulus (element (i,j) of plane t at t*Np*Mp + j*Mp + i).
+ */
+#ifndef OZAKI_H
+#define OZAKI_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OZ_OK = 0,
+  OZ_EINVAL = -1,   /* invalid argument (dimension, leading dimension, count, null) */
+  OZ_ERANGE = -2,   /* too few moduli for this k: k_A would be < 1 */
+  OZ_ECUDA = -3,    /* a CUDA runtime call or kernel launch failed */
+  OZ_ENOMEM = -4,   /* workspace allocation failed or the given workspace is too small */
+  OZ_ETIMEOUT = -5, /* device side: a bounded wait in a kernel expired (status word) */
+  OZ_ENODEV = -6    /* no usable sm_103 device */
+} oz_status;
+
+#define OZ_MAX_MODULI 20
+#define OZ_MIN_MODULI 2
+#define OZ_MAX_SLICES 20
+#define OZ_EXP_EMPTY ((int32_t)0x80808080)
+#define OZ_EXP_NONFINITE ((int32_t)0x7fffffff)
+
+/* ---------------------------------------------------------------- host-only queries */
+
+/* The first num_moduli moduli of the greedy descending pairwise-coprime list starting
+ * at 256 ([Ozaki II] sections 4 and 6: 2 <= m_t <= 256, pairwise coprime).  Writes
+ * num_moduli ints to moduli_out (host memory).  OZ_EINVAL if num_moduli is outside
+ * [1, OZ_MAX_MODULI] or moduli_out is NULL.  No GPU needed. */
+int ozaki2_moduli(int num_moduli, int* moduli_out);
+
+/* k_A = k_B of [Ozaki II] section 5: the largest integer k with
+ * k_inner * 2^(2k) <= M/2 - 1, M the product of the moduli.  *k_out receives it.
+ * OZ_ERANGE if no k >= 1 exists.  No GPU needed. */
+int ozaki2_choose_k(int num_moduli, long long k_inner, int* k_out);
+
+/* Padded plane dimensions Mp, Np, Kp (see the layout above).  No GPU needed. */
+int ozaki2_plane_dims(int m, int n, int k, int* mp, int* np, int* kp);
+
+/* Bytes of device workspace ozaki2_dgemm_ws needs (0 on invalid arguments). */
+size_t ozaki2_workspace_bytes(int m, int n, int k, int num_moduli);
+
+/* ---------------------------------------------------------------- Scheme II steps */
+
+/* Step a1 ([Ozaki II] section 3 and Algorithm 1 step 2, the choice of D and E):
+ * rowexp[i] = max_j ceil(log2 |a_ij|), colexp[j] = max_l ceil(log2 |b_lj|), with the
+ * markers OZ_EXP_EMPTY / OZ_EXP_NONFINITE.  rowexp has m ints, colexp n ints. */
+int ozaki2_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                     int32_t* rowexp, int32_t* colexp, cudaStream_t stream);
+
+/* Step a2 (Algorithm 1 steps 2-3, left half): A' = trunc(D A) with
+ * D_ii = 2^(k_A - rowexp[i]), B' = trunc(B E) likewise, then the symmetric residues
+ * mod each of the first num_moduli moduli, written as bf16 planes (layout above).
+ * Either operand may be skipped by passing NULL for its source and planes. */
+int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                 int num_moduli, const int32_t* rowexp, const int32_t* colexp,
+                 uint16_t* A_planes, uint16_t* B_planes, cudaStream_t stream);
+
+/* Steps a3+a4 (Algorithm 1 step 3): for every modulus t, the exact integer product
+ * C'_t = A'_t B'_t on the tensor cores and C''_t = C'_t mod m_t, written to C_res.
+ * Exact for every k (the k loop is folded mod m_t every 960 terms). */
+int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_planes,
+                        const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
+
+/* Steps a5+a6 (Algorithm 1 steps 4-6): Z = sum_t C''_t M_t y_t, C''' = Z mod M (the
+ * symmetric representative), C_ij = RN(C'''_ij * 2^-(d_i + e_j)) with one rounding
+ * (round-to-nearest-even, subnormals included, +-inf on overflow). */
+int ozaki2_crt(int m, int n, int k, int num_moduli, const uint8_t* C_res,
+               const int32_t* rowexp, const int32_t* colexp, double* C, int ldc,
+               cudaStream_t stream);
+
+/* ---------------------------------------------------------------- Scheme II, composed */
+
+/* C = A*B by Ozaki Scheme II with num_moduli in [OZ_MIN_MODULI, OZ_MAX_MODULI] moduli,
+ * using the caller's device workspace (ws_bytes >= ozaki2_workspace_bytes(...), base
+ * aligned to 256 bytes).  OZ_ENOMEM if the workspace is too small. */
+int ozaki2_dgemm_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    double* C, int ldc, int num_moduli, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* Same, with the workspace taken from and returned to the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).  On first use per device the library
+ * raises the release threshold of that device's default memory pool so freed
+ * workspace stays cached for the next call (a process-wide setting of that pool). */
+int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                 double* C, int ldc, int num_moduli, cudaStream_t stream);
+
+/* Same with HOST pointers: copies A and B to the current device, computes, copies C
+ * back and synchronises before returning (a drop-in CPU-callable DGEMM). */
+int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                      double* C, int ldc, int num_moduli);
+
+/* ---------------------------------------------------------------- status */
+
+/* Synchronises the current device, returns the device status word (OZ_OK or
+ * OZ_ETIMEOUT from a kernel's bounded wait) and clears it.  OZ_ECUDA if the
+ * synchronisation itself fails. */
+int ozaki_get_device_status(void);
+
+/* Human-readable name of a status code (static string). */
+const char* ozaki_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OZAKI_H */

@@ -1,0 +1,98 @@
+"""The C-ABI library loads and exports what include/ozaki.h declares; host logic matches the oracle.
+
+No GPU is used here: only host-side queries and argument checks that return before
+any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp64_gemm_emulation_gb300 import build_lib
+from oracle import ozaki2 as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def oz():
+    if not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    from fp64_gemm_emulation_gb300 import ozaki
+
+    return ozaki
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            with open(os.path.join(ROOT, "include", hdr)) as f:
+                names += re.findall(r"^(?:int|size_t|const char\*)\s+(\w+)\s*\(", f.read(), flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(oz):
+    names = declared_functions()
+    assert len(names) >= 13
+    lib = ctypes.CDLL(build_lib.LIB)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_moduli_match_the_oracle(oz):
+    for s in range(1, 21):
+        assert oz.ozaki2_moduli(s) == O.greedy_moduli(s)
+
+
+@pytest.mark.parametrize("s", [2, 3, 8, 10, 12, 14, 16, 18, 20])
+@pytest.mark.parametrize("q", [1, 63, 256, 960, 4096, 8192, 16384, 131071, 131072, 262144, 2**31 - 1])
+def test_choose_k_matches_the_oracle(oz, s, q):
+    M = O.crt_constants(O.greedy_moduli(s)).M
+    try:
+        want = O.choose_k(M, q)
+    except ValueError:
+        want = None
+    if want is None or want < 1:
+        with pytest.raises(oz.OzakiError) as e:
+            oz.ozaki2_choose_k(s, q)
+        assert e.value.code == oz.OZ_ERANGE
+    else:
+        assert oz.ozaki2_choose_k(s, q) == want
+
+
+def test_plane_dims_and_workspace(oz):
+    assert oz.ozaki2_plane_dims(1, 1, 1) == (256, 256, 64)
+    assert oz.ozaki2_plane_dims(300, 520, 2100) == (512, 768, 2112)
+    assert oz.ozaki2_plane_dims(16384, 16384, 16384) == (16384, 16384, 16384)
+    ws = oz.ozaki2_workspace_bytes(300, 520, 2100, 14)
+    assert ws >= 14 * (512 + 768) * 2112 * 2 + 14 * 512 * 768
+    assert oz.ozaki2_workspace_bytes(300, 520, 2100, 1) == 0   # fewer than 2 moduli
+    assert oz.ozaki2_workspace_bytes(-1, 5, 5, 14) == 0
+
+
+def test_argument_errors_are_synchronous(oz):
+    lib = oz._lib
+    null = None
+    # negative dimension, bad leading dimensions, moduli count out of range
+    assert lib.ozaki2_dgemm(-1, 4, 4, null, 1, null, 4, null, 1, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm(8, 4, 4, null, 7, null, 4, null, 8, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm(8, 4, 4, null, 8, null, 3, null, 8, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm(8, 4, 4, null, 8, null, 4, null, 7, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm(8, 4, 4, null, 8, null, 4, null, 8, 1, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm(8, 4, 4, null, 8, null, 4, null, 8, 21, null) == oz.OZ_EINVAL
+    # empty problems return at once
+    assert lib.ozaki2_dgemm(0, 4, 4, null, 1, null, 4, null, 1, 14, null) == oz.OZ_OK
+    assert lib.ozaki2_dgemm(4, 0, 4, null, 4, null, 4, null, 4, 14, null) == oz.OZ_OK
+    # too few moduli for the inner dimension
+    assert lib.ozaki2_dgemm_ws(8, 8, 2**30, 1, 8, 1, 2**30, 1, 8, 2, 1, 1 << 40, null) == oz.OZ_ERANGE
+    # workspace too small
+    assert lib.ozaki2_dgemm_ws(8, 8, 8, 1, 8, 1, 8, 1, 8, 14, 256, 16, null) == oz.OZ_ENOMEM
+    assert oz.ozaki_status_string(oz.OZ_ETIMEOUT).startswith("OZ_ETIMEOUT")
+
+
+def test_binding_names_follow_the_header(oz):
+    for name in declared_functions():
+        if name.startswith("ozaki"):
+            assert hasattr(oz, name), name

@@ -1,0 +1,209 @@
+"""GPU path vs the CPU oracle, element by element, through the C ABI (Scheme II).
+
+Bar: bit-exact everywhere.  Exponents, residue planes and C''_t are integer data;
+the final C is the single rounding of an exact integer, which both sides take
+the same way, so C is compared bit for bit as well (the benchmark spec's tolerance
+|dC| <= 2^-50 (|A||B|) is checked on top as a sanity bound).
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from fp64_gemm_emulation_gb300.inputs import hpl_like, special_matrix
+from oracle import ozaki2 as O
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def oz():
+    from fp64_gemm_emulation_gb300 import ozaki
+
+    return ozaki
+
+
+def dev(X):
+    """Column-major float64 CUDA tensor from a numpy array."""
+    X = np.asfortranarray(X, dtype=np.float64)
+    return torch.from_numpy(X.T.copy()).cuda().t()
+
+
+def host(T):
+    return T.t().contiguous().cpu().numpy().T
+
+
+def exps_as_int32(E):
+    out = []
+    for e in E:
+        if e is O.ZERO_ROW:
+            out.append(int(np.int32(np.uint32(0x80808080).view(np.int32))))
+        elif e == "nan":
+            out.append(0x7FFFFFFF)
+        else:
+            out.append(e)
+    return np.array(out, dtype=np.int32)
+
+
+def exact_entry(A, B, i, j):
+    """(AB)_ij exactly, as a Fraction."""
+    return sum((Fraction(float(a)) * Fraction(float(b)) for a, b in zip(A[i, :], B[:, j])), Fraction(0))
+
+
+def bits(x):
+    return np.ascontiguousarray(x, dtype=np.float64).view(np.int64)
+
+
+def bf16_planes_to_int(P):
+    """bf16 bit patterns (int16 tensor) -> integer values."""
+    u = P.cpu().numpy().astype(np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.int64)
+
+
+# ------------------------------------------------------------------ step by step
+STEP_CASES = [
+    # m, n, k, s, phi, seed
+    (256, 256, 256, 14, 0.5, 0),      # the 256^3 workload
+    (300, 520, 2100, 14, 0.5, 1),     # several tiles, ragged, 3 k-chunks
+    (129, 257, 961, 8, 2.0, 2),       # one past every tile edge, 2 chunks
+    (64, 40, 960, 16, 0.0, 3),        # exactly one chunk
+    (200, 300, 3000, 20, 4.0, 4),     # widest exponent spread, 20 moduli, 4 chunks
+    (17, 9, 5, 2, 0.5, 5),            # tiny, 2 moduli
+]
+
+
+@pytest.mark.parametrize("m,n,k,s,phi,seed", STEP_CASES)
+def test_steps_bit_exact(oz, m, n, k, s, phi, seed):
+    A, B = hpl_like(m, n, k, phi=phi, seed=seed)
+    ref = O.ozaki2_dgemm(A, B, s)
+    dA, dB = dev(A), dev(B)
+
+    rowexp, colexp = oz.ozaki2_exponents(dA, dB)
+    assert np.array_equal(rowexp.cpu().numpy(), exps_as_int32(ref.EA))
+    assert np.array_equal(colexp.cpu().numpy(), exps_as_int32(ref.EB))
+
+    Ap, Bp = oz.ozaki2_split(dA, dB, s, rowexp, colexp)
+    Ai, Bi = bf16_planes_to_int(Ap), bf16_planes_to_int(Bp)
+    assert np.array_equal(Ai[:, :m, :k], ref.Ares.astype(np.int64))
+    assert np.array_equal(Bi[:, :n, :k], np.transpose(ref.Bres, (0, 2, 1)).astype(np.int64))
+    assert not Ai[:, m:, :].any() and not Ai[:, :, k:].any()      # zero padding
+    assert not Bi[:, n:, :].any() and not Bi[:, :, k:].any()
+
+    Cr = oz.ozaki2_residue_gemm(m, n, k, s, Ap, Bp)
+    got = Cr.cpu().numpy()[:, :n, :m]                               # [s][j][i]
+    assert np.array_equal(got, np.transpose(ref.Cres, (0, 2, 1)).astype(np.uint8))
+
+    C = oz.ozaki2_crt(m, n, k, s, Cr, rowexp, colexp)
+    assert np.array_equal(bits(host(C)), bits(ref.C))
+    assert oz.ozaki_get_device_status() == oz.OZ_OK
+
+
+# ------------------------------------------------------------------ whole call
+E2E_CASES = [
+    (256, 256, 256, 14, 0.5, 0),
+    (333, 444, 1234, 14, 1.0, 6),
+    (96, 80, 70, 10, 0.5, 7),
+    (511, 257, 1919, 12, 2.0, 8),
+]
+
+
+@pytest.mark.parametrize("m,n,k,s,phi,seed", E2E_CASES)
+def test_dgemm_bit_exact(oz, m, n, k, s, phi, seed):
+    A, B = hpl_like(m, n, k, phi=phi, seed=seed)
+    ref = O.ozaki2_dgemm(A, B, s, keep=False).C
+    C = oz.ozaki2_dgemm(dev(A), dev(B), s)
+    assert np.array_equal(bits(host(C)), bits(ref))
+    if s >= 14:  # spec floor |dC| <= 2^-50 (|A||B|), on sampled entries vs the exact product
+        Ch = host(C)
+        rng = np.random.default_rng(seed)
+        for i, j in zip(rng.integers(0, m, 16), rng.integers(0, n, 16)):
+            exact = exact_entry(A, B, i, j)
+            bound = Fraction(float(np.abs(A[i]) @ np.abs(B[:, j]))) * Fraction(2) ** -50
+            assert abs(Fraction(float(Ch[i, j])) - exact) <= bound
+
+
+@pytest.mark.parametrize("s", list(range(2, 21)))
+def test_every_moduli_count(oz, s):
+    m, n, k = 70, 90, 40
+    A, B = hpl_like(m, n, k, phi=0.5, seed=100 + s)
+    ref = O.ozaki2_dgemm(A, B, s, keep=False).C
+    C = oz.ozaki2_dgemm(dev(A), dev(B), s)
+    assert np.array_equal(bits(host(C)), bits(ref))
+
+
+@pytest.mark.parametrize("kind", ["zeros", "pow2", "subnormal", "zero_rows", "ints", "huge"])
+def test_special_inputs(oz, kind):
+    A = special_matrix(kind, 130, 270, seed=11)
+    B = special_matrix(kind if kind != "huge" else "pow2", 270, 70, seed=12)
+    ref = O.ozaki2_dgemm(A, B, 14, keep=False).C
+    C = oz.ozaki2_dgemm(dev(A), dev(B), 14)
+    assert np.array_equal(bits(host(C)), bits(ref))
+
+
+def test_overflow_and_underflow_edges(oz):
+    # products beyond DBL_MAX give inf; products far below the subnormal range give 0
+    A = np.asfortranarray(np.full((3, 2), 2.0**600))
+    B = np.asfortranarray(np.array([[2.0**500, 2.0**-700, -(2.0**-1000)], [2.0**500, 2.0**-700, 0.0]]))
+    A[2, :] = [2.0**-600, -(2.0**-600)]
+    ref = O.ozaki2_dgemm(A, B, 14, keep=False).C
+    C = oz.ozaki2_dgemm(dev(A), dev(B), 14)
+    assert np.array_equal(bits(host(C)), bits(ref))
+    assert np.isinf(ref[0, 0])
+
+
+def test_non_finite_inputs(oz):
+    A, B = hpl_like(40, 30, 50, seed=13)
+    A[5, 7] = np.inf
+    A[9, 0] = np.nan
+    B[3, 11] = -np.inf
+    ref = O.ozaki2_dgemm(A, B, 14, keep=False).C
+    C = host(oz.ozaki2_dgemm(dev(A), dev(B), 14))
+    assert np.array_equal(bits(C), bits(ref))
+    assert np.isnan(C[5]).all() and np.isnan(C[:, 11]).all()
+
+
+def test_k_zero_gives_zeros(oz):
+    dA = torch.empty((5, 0), dtype=torch.float64, device="cuda")
+    dB = torch.empty((0, 4), dtype=torch.float64, device="cuda")
+    C = torch.full((4, 5), 7.0, dtype=torch.float64, device="cuda").t()
+    lib = oz._lib
+    rc = lib.ozaki2_dgemm(5, 4, 0, dA.data_ptr(), 5, dB.data_ptr(), 1, C.data_ptr(), 5, 14,
+                          torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    assert np.all(bits(host(C)) == 0)
+
+
+def test_leading_dimensions_and_views(oz):
+    m, n, k = 150, 130, 300
+    A, B = hpl_like(m, n, k, seed=14)
+    big_A = np.zeros((m + 13, k), order="F")
+    big_A[:m] = A
+    big_B = np.zeros((k + 5, n), order="F")
+    big_B[:k] = B
+    dA = dev(big_A)[:m]
+    dB = dev(big_B)[:k]
+    Cbig = torch.full((n, m + 7), -1.0, dtype=torch.float64, device="cuda").t()
+    C = oz.ozaki2_dgemm(dA, dB, 14, C=Cbig[:m])
+    ref = O.ozaki2_dgemm(A, B, 14, keep=False).C
+    assert np.array_equal(bits(host(C)), bits(ref))
+    assert torch.all(Cbig[m:] == -1.0)          # padding rows of C untouched
+
+
+def test_ws_and_host_variants_agree(oz):
+    m, n, k = 200, 210, 900
+    A, B = hpl_like(m, n, k, seed=15)
+    ref = O.ozaki2_dgemm(A, B, 14, keep=False).C
+    ws = torch.empty(oz.ozaki2_workspace_bytes(m, n, k, 14), dtype=torch.uint8, device="cuda")
+    C1 = host(oz.ozaki2_dgemm_ws(dev(A), dev(B), 14, ws))
+    C2 = oz.ozaki2_dgemm_host(A, B, 14)
+    assert np.array_equal(bits(C1), bits(ref))
+    assert np.array_equal(bits(C2), bits(ref))
+
+
+def test_deterministic_repeats(oz):
+    A, B = hpl_like(640, 520, 2000, seed=16)
+    dA, dB = dev(A), dev(B)
+    outs = [bits(host(oz.ozaki2_dgemm(dA, dB, 14))) for _ in range(3)]
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
