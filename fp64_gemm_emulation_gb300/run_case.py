@@ -1,0 +1,69 @@
+"""Run the Scheme II path on one problem size (for profiling and quick timing).
+
+    python -m fp64_gemm_emulation_gb300.run_case --m 4096 --n 4096 --k 4096 --moduli 14 --reps 3
+
+Runs the four steps (exponents, split, residue GEMM, CRT) through the C ABI on
+HPL-like inputs resident on the GPU, ``--reps`` times, and prints per-step CUDA-event
+times of the last repetition.
+"""
+from __future__ import annotations
+
+import argparse
+
+import numpy as np
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--m", type=int, default=4096)
+    ap.add_argument("--n", type=int, default=4096)
+    ap.add_argument("--k", type=int, default=4096)
+    ap.add_argument("--moduli", type=int, default=14)
+    ap.add_argument("--phi", type=float, default=0.5)
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args()
+
+    import torch
+
+    from fp64_gemm_emulation_gb300 import ozaki as oz
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+
+    m, n, k, s = a.m, a.n, a.k, a.moduli
+    A, B = hpl_like(m, n, k, phi=a.phi, seed=0)
+    dA = torch.from_numpy(A.T.copy()).cuda().t()
+    dB = torch.from_numpy(B.T.copy()).cuda().t()
+    dC = torch.empty((n, m), dtype=torch.float64, device="cuda").t()
+    mp, np_, kp = oz.ozaki2_plane_dims(m, n, k)
+    rowexp = torch.empty(m, dtype=torch.int32, device="cuda")
+    colexp = torch.empty(n, dtype=torch.int32, device="cuda")
+    Ap = torch.empty((s, mp, kp), dtype=torch.int16, device="cuda")
+    Bp = torch.empty((s, np_, kp), dtype=torch.int16, device="cuda")
+    Cr = torch.empty((s, np_, mp), dtype=torch.uint8, device="cuda")
+    lib, st = oz._lib, torch.cuda.current_stream().cuda_stream
+    p = lambda t: t.data_ptr()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for _ in range(a.reps):
+        ev[0].record()
+        rc = lib.ozaki2_exponents(m, n, k, p(dA), m, p(dB), k, p(rowexp), p(colexp), st)
+        ev[1].record()
+        rc |= lib.ozaki2_split(m, n, k, p(dA), m, p(dB), k, s, p(rowexp), p(colexp), p(Ap), p(Bp), st)
+        ev[2].record()
+        rc |= lib.ozaki2_residue_gemm(m, n, k, s, p(Ap), p(Bp), p(Cr), st)
+        ev[3].record()
+        rc |= lib.ozaki2_crt(m, n, k, s, p(Cr), p(rowexp), p(colexp), p(dC), m, st)
+        ev[4].record()
+        if rc:
+            raise SystemExit(f"ozaki call failed: {rc}")
+    torch.cuda.synchronize()
+    status = oz.ozaki_get_device_status()
+    names = ["exponents", "split", "residue_gemm", "crt"]
+    t = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+    print(f"{m}x{n}x{k} s={s}: " + ", ".join(f"{nm} {x:.3f} ms" for nm, x in zip(names, t))
+          + f"; gemm {s * 2.0 * m * n * k / (t[2] * 1e-3) / 1e12:.1f} TFLOP/s; status {status}")
+    if status:
+        raise SystemExit(1)
+    return np.float64(sum(t))
+
+
+if __name__ == "__main__":
+    main()
