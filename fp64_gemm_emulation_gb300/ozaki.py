@@ -23,6 +23,7 @@ OZ_OK, OZ_EINVAL, OZ_ERANGE, OZ_ECUDA, OZ_ENOMEM, OZ_ETIMEOUT, OZ_ENODEV = 0, -1
 OZ_EXP_EMPTY = np.int32(np.uint32(0x80808080).view(np.int32))
 OZ_EXP_NONFINITE = np.int32(0x7FFFFFFF)
 PAD_M, PAD_N, PAD_K = 256, 256, 64
+OZ_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class OzakiError(RuntimeError):
@@ -48,6 +49,7 @@ def _load():
         "ozaki2_dgemm_ws": (I, [I, I, I, P, I, P, I, P, I, I, P, S, P]),
         "ozaki2_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
         "ozaki2_dgemm_host": (I, [I, I, I, P, I, P, I, P, I, I]),
+        "ozaki2_dgemm_noalloc": (I, [I, I, I, P, I, P, I, P, I, I, P]),
         "ozaki_get_device_status": (I, []),
         "ozaki_status_string": (ctypes.c_char_p, [I]),
     }
@@ -187,6 +189,20 @@ def ozaki2_dgemm_ws(A, B, num_moduli: int, workspace, C=None, stream=None):
     _check(_lib.ozaki2_dgemm_ws(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli,
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "ozaki2_dgemm_ws")
+    return C
+
+
+def ozaki2_dgemm_noalloc(A, B, num_moduli: int = 14, C=None, stream=None):
+    """C = A B without any device allocation: the library's fixed 64 MiB scratch buffer
+    holds the workspace (for callers that cannot allocate; see include/ozaki.h)."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    _check(_lib.ozaki2_dgemm_noalloc(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli,
+                                     _stream(stream)), "ozaki2_dgemm_noalloc")
     return C
 
 

@@ -134,6 +134,26 @@ int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
 int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                       double* C, int ldc, int num_moduli);
 
+/* ---------------------------------------------------------------- without allocation */
+
+/* Size of the fixed scratch buffer ozaki2_dgemm_noalloc uses (64 MiB). */
+#define OZ_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* C = A*B like ozaki2_dgemm, for callers that cannot allocate device memory when they
+ * multiply (for example a process whose memory manager owns the whole GPU, or a loop
+ * that must not allocate after start-up).  The pages have no counterpart: this is a
+ * library convenience.  Nothing is allocated: the workspace is a fixed buffer of
+ * OZ_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ * holds until the process exits.  Problems whose ozaki2_workspace_bytes(m, n, k,
+ * num_moduli) exceeds it are rejected with OZ_ENOMEM before anything runs (at 14 moduli
+ * m = n = k = 768 fits, 1024 does not).  The first call on each device looks up the
+ * buffer's device address (with that device current); make that first call before any
+ * stream capture.  All calls share the one buffer, which keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other threads) race on it.
+ * Same arguments, ordering and errors as ozaki2_dgemm otherwise. */
+int ozaki2_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                         double* C, int ldc, int num_moduli, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- status */
 
 /* Synchronises the current device, returns the device status word (OZ_OK or
