@@ -11,13 +11,14 @@
 // (tcgen05.ld -> exact float remainder -> tcgen05.st), so the next chunk accumulates
 // on a value in [0, m_t).  Two accumulators alternate so the tensor cores keep
 // running while one is being reduced.  The last two chunks of a tile are not written
-// back: their residues are combined in the uint8 output plane (store, then add mod m).
+// back: the first one's residues are kept in a shared-memory tile, the second one's are
+// added to them mod m_t, and the finished uint8 tile leaves with coalesced 16-byte stores.
 // This replaces the pages' block multiplication for k >= 2^17: the result is exact
 // for every k.
 //
 // Kernel shape (one CTA per SM, persistent over work units (tile, modulus)):
 //   tile 128 x 256 (UMMA M=128, N=256, K=16), stage = 64 k (128-byte rows, 128B swizzle)
-//   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer   warps 2-5: epilogue
+//   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer   warps 2-9: epilogue
 //   TMEM: 512 columns = two 128 x 256 FP32 accumulators.
 // Every mbarrier wait is bounded (oz::mbar_wait); on expiry the CTA records
 // OZ_ETIMEOUT in the device status word, drains what it issued and returns.
@@ -38,9 +39,12 @@ constexpr int KB_PER_CHUNK = 15;  // 960 k per exactly-representable chunk
 constexpr uint32_t A_STAGE = BM * BK * 2;
 constexpr uint32_t B_STAGE = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                 // two per SM sub-partition
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int THREADS = 64 + EPI_THREADS;   // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t TMEM_COLS = 512;
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+constexpr uint32_t STASH_BYTES = BM * BN;   // one uint8 residue tile, [col][row]
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + STASH_BYTES + 256 /*barriers*/;
 constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
 static_assert(255 + KB_PER_CHUNK * BK * 128 * 128 <= (1 << 24), "chunk too long for exact FP32 sums");
 }  // namespace gemm
@@ -58,13 +62,28 @@ __device__ __forceinline__ void record_timeout(volatile int* abort_flag) {
   atomicExch(&g_status, OZ_ETIMEOUT);
 }
 
-// Exact remainder of an integer-valued float v (|v| < 2^25) modulo m, in [0, m).
+// Exact remainder of an integer-valued float v (|v| < 2^25) modulo m (173 <= m <= 256),
+// in [0, m).  q is v/m rounded to an integer by the 1.5 * 2^23 magic constant (|v/m| <
+// 2^22); it is floor(v/m) or one more, so v - q m is exact and lies in (-m, m).
 __device__ __forceinline__ float exact_mod(float v, float m, float inv_m) {
-  const float q = floorf(v * inv_m);  // within 1 of floor(v/m)
-  float r = fmaf(-q, m, v);           // exact: the true value is a small integer
-  r = (r < 0.0f) ? r + m : r;
-  r = (r >= m) ? r - m : r;
-  return r;
+  const float q = fmaf(v, inv_m, 12582912.0f) - 12582912.0f;
+  const float r = fmaf(-q, m, v);
+  return r < 0.0f ? r + m : r;
+}
+
+// Low 8 bits of a float holding an integer in [0, 256).
+__device__ __forceinline__ uint32_t small_float_to_u8(float r) {
+  return __float_as_uint(r + 8388608.0f) & 0xFFu;
+}
+
+// Rendezvous of the epilogue warps on an mbarrier (one arrival per warp), with the same
+// bounded wait as every other wait in the kernel.  Returns false on expiry.
+__device__ __forceinline__ bool epilogue_sync(uint64_t* bar, uint32_t& phase) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase);
+  phase ^= 1;
+  return ok;
 }
 
 struct UnitCoord {
@@ -97,13 +116,15 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* stash = smem + STAGES * STAGE_BYTES;  // [BN][BM] uint8 residues
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stash + STASH_BYTES);
   uint64_t* full = bars;                  // [STAGES]  TMA -> MMA
   uint64_t* empty = bars + STAGES;        // [STAGES]  MMA -> TMA
   uint64_t* accfull = bars + 2 * STAGES;  // [2]       MMA -> epilogue
   uint64_t* accempty = accfull + 2;       // [2]       epilogue -> MMA
   uint64_t* drain = accempty + 2;         // [1]       MMA drain on the error path
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epibar = drain + 1;           // [1]       epilogue warps rendezvous
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epibar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,9 +139,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], 4);
+      mbar_init(&accempty[i], EPI_WARPS);
     }
     mbar_init(drain, 1);
+    mbar_init(epibar, EPI_WARPS);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
@@ -217,17 +239,19 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       if (!mbar_wait(drain, 0)) record_timeout(abort_flag);
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2-5)
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-    const int row_in_tile = quad * 32 + lane;
+    // ------------------------------------------------------------ epilogue (warps 2-9)
+    // Thread = one accumulator row (TMEM lane) and one half of the 256 columns.
+    const int quad = warp & 3;             // TMEM lanes 32*quad .. 32*quad+31
+    const int half = (warp - 2) >> 2;      // columns [128*half, 128*half + 128)
+    const int row = quad * 32 + lane;
+    const int etid = threadIdx.x - 64;     // 0 .. EPI_THREADS-1
     const long long plane = static_cast<long long>(np) * mp;
-    uint32_t g = 0;
+    uint32_t g = 0, eph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
       const float mf = c.modf[uc.t], inv = c.invf[uc.t];
       const uint32_t mi = static_cast<uint32_t>(mf);
-      uint8_t* out = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM + row_in_tile;
       for (int ch = 0; ch < nchunks; ++ch, ++g) {
         const uint32_t acc = g & 1;
         if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
@@ -236,28 +260,33 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
         const bool final_chunk = (ch + 2 >= nchunks);
-        const bool first_final = final_chunk && (ch == 0 || ch == nchunks - 2);
+        const bool combine = final_chunk && (ch == nchunks - 1) && (nchunks >= 2);
 #pragma unroll 1
-        for (int cb = 0; cb < BN / 32; ++cb) {
-          uint32_t v[32];
-          tmem_ld32(taddr + cb * 32, v);
+        for (int cb = 0; cb < 128; cb += 64) {
+          uint32_t v[32], w[32];
+          tmem_ld32(taddr + cb, v);
+          tmem_ld32(taddr + cb + 32, w);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
+          for (int i = 0; i < 32; ++i) {
+            v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
+            w[i] = __float_as_uint(exact_mod(__uint_as_float(w[i]), mf, inv));
+          }
           if (!final_chunk) {
-            tmem_st32(taddr + cb * 32, v);
+            tmem_st32(taddr + cb, v);
+            tmem_st32(taddr + cb + 32, w);
           } else {
-            uint8_t* o = out + static_cast<long long>(cb * 32) * mp;
+            uint8_t* col0 = stash + (half * 128 + cb) * BM + row;  // [col][row]
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              uint32_t r = static_cast<uint32_t>(__uint_as_float(v[i]));
-              if (!first_final) {
-                r += o[static_cast<long long>(i) * mp];
-                if (r >= mi) r -= mi;
+            for (int i = 0; i < 64; ++i) {
+              uint32_t r = small_float_to_u8(__uint_as_float(i < 32 ? v[i] : w[i - 32]));
+              if (combine) {
+                r += col0[i * BM];
+                r = (r >= mi) ? r - mi : r;
               }
-              o[static_cast<long long>(i) * mp] = static_cast<uint8_t>(r);
+              col0[i * BM] = static_cast<uint8_t>(r);
             }
           }
         }
@@ -265,6 +294,25 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&accempty[acc]);
+      }
+      if (!ok) break;
+      // The finished tile is in the stash: copy it out with coalesced 16-byte stores
+      // (column j of the tile is 128 contiguous bytes of plane t).
+      if (!epilogue_sync(epibar, eph)) {
+        if (lane == 0) record_timeout(abort_flag);
+        break;
+      }
+      uint8_t* dst = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM;
+#pragma unroll
+      for (int i = 0; i < (BN * BM / 16) / EPI_THREADS; ++i) {
+        const int q = etid + i * EPI_THREADS;
+        const int col = q >> 3, part = q & 7;
+        *reinterpret_cast<uint4*>(dst + static_cast<long long>(col) * mp + part * 16) =
+            *reinterpret_cast<const uint4*>(stash + col * BM + part * 16);
+      }
+      if (!epilogue_sync(epibar, eph)) {
+        if (lane == 0) record_timeout(abort_flag);
+        break;
       }
     }
   }
