@@ -41,7 +41,8 @@ __device__ __forceinline__ bool any_below(const uint32_t (&x)[kLimbs], int pos) 
   return any;
 }
 
-// RN-even of (-1)^neg * mag * 2^-D as IEEE-754 binary64 bits.
+// RN-even of (-1)^neg * mag * 2^-D as IEEE-754 binary64 bits (mag: 6 limbs, any above
+// the caller's limb count zero).
 __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLimbs], bool neg, int D) {
   int L = 0;  // bit length of mag
 #pragma unroll
@@ -77,99 +78,134 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLim
   return bits | (neg ? 0x8000000000000000ull : 0ull);
 }
 
+// One thread = 4 consecutive rows i of one column j (a 4-byte load per modulus).
+// NL = 32-bit limbs needed for Z = sum_t c_t P_t (< 255 s M).
+template <int NL>
 __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c,
                                                   const uint8_t* __restrict__ C_res,
                                                   const int32_t* __restrict__ rowexp,
                                                   const int32_t* __restrict__ colexp, double* __restrict__ C,
                                                   long long ldc) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= m) return;
+  const int i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (i0 >= m) return;
   const long long plane = static_cast<long long>(np) * mp;
-  const int E = __ldg(rowexp + i);
+  int E[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) E[e] = (i0 + e < m) ? __ldg(rowexp + i0 + e) : OZ_EXP_EMPTY;
   for (int j = blockIdx.y; j < n; j += gridDim.y) {
     const int F = __ldg(colexp + j);
-    double* out = C + i + j * ldc;
-    if (E == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) {
-      *out = __longlong_as_double(0x7FF8000000000000ll);
-      continue;
-    }
-    if (E == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) {
-      *out = 0.0;
-      continue;
-    }
-    uint64_t acc[kLimbs];
+    // all residues of the 4 elements first: s independent 4-byte loads in flight
+    uint32_t res[kMaxModuli];
+    const uint8_t* base = C_res + static_cast<long long>(j) * mp + i0;
 #pragma unroll
-    for (int l = 0; l < kLimbs; ++l) acc[l] = 0;
-    uint64_t qs = 0;
-    const uint8_t* res = C_res + static_cast<long long>(j) * mp + i;
-#pragma unroll 4
-    for (int t = 0; t < c.s; ++t) {
-      const uint32_t r = __ldg(res + t * plane);
+    for (int t = 0; t < kMaxModuli; ++t)
+      res[t] = (t < c.s) ? __ldg(reinterpret_cast<const uint32_t*>(base + t * plane)) : 0u;
+    double* out = C + i0 + j * ldc;
+#pragma unroll 1
+    for (int e = 0; e < 4; ++e) {
+      if (i0 + e >= m) break;
+      if (E[e] == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) {
+        out[e] = __longlong_as_double(0x7FF8000000000000ll);
+        continue;
+      }
+      if (E[e] == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) {
+        out[e] = 0.0;
+        continue;
+      }
+      uint64_t acc[NL];
 #pragma unroll
-      for (int l = 0; l < kLimbs; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
-      qs += static_cast<uint64_t>(r) * c.frac[t];
-    }
-    // Z in 32-bit limbs
-    uint32_t z[kLimbs];
-    uint64_t carry = 0;
+      for (int l = 0; l < NL; ++l) acc[l] = 0;
+      uint64_t qs = 0;
 #pragma unroll
-    for (int l = 0; l < kLimbs; ++l) {
-      const uint64_t v = acc[l] + carry;
-      z[l] = static_cast<uint32_t>(v);
-      carry = v >> 32;
-    }
-    // X = Z - Q M  (two's complement)
-    const uint32_t Q = static_cast<uint32_t>((qs + 0x80000000ull) >> 32);
-    uint32_t x[kLimbs];
-    uint64_t qc = 0;
-    uint32_t borrow = 0;
+      for (int t = 0; t < kMaxModuli; ++t) {
+        if (t < c.s) {
+          const uint32_t r = (res[t] >> (8 * e)) & 0xFFu;
 #pragma unroll
-    for (int l = 0; l < kLimbs; ++l) {
-      const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
-      qc = qm >> 32;
-      const uint64_t d = static_cast<uint64_t>(z[l]) - static_cast<uint32_t>(qm) - borrow;
-      x[l] = static_cast<uint32_t>(d);
-      borrow = static_cast<uint32_t>(d >> 63);
-    }
-    bool neg = (x[kLimbs - 1] >> 31) != 0;
-    if (neg) {  // magnitude
-      uint32_t cy = 1;
+          for (int l = 0; l < NL; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
+          qs += static_cast<uint64_t>(r) * c.frac[t];
+        }
+      }
+      // Z in 32-bit limbs
+      uint32_t x[kLimbs];
+      uint64_t carry = 0;
 #pragma unroll
-      for (int l = 0; l < kLimbs; ++l) {
-        const uint64_t v = static_cast<uint64_t>(~x[l]) + cy;
+      for (int l = 0; l < NL; ++l) {
+        const uint64_t v = acc[l] + carry;
         x[l] = static_cast<uint32_t>(v);
-        cy = static_cast<uint32_t>(v >> 32);
+        carry = v >> 32;
       }
-    }
-    // one correction: if |X| > M/2 the representative is M - |X| with the other sign
-    bool gt = false, decided = false;
+      // X = Z - Q M  (two's complement over NL limbs)
+      const uint32_t Q = static_cast<uint32_t>((qs + 0x80000000ull) >> 32);
+      uint64_t qc = 0;
+      uint32_t borrow = 0;
 #pragma unroll
-    for (int l = kLimbs - 1; l >= 0; --l) {
-      if (!decided && x[l] != c.halfM[l]) {
-        gt = x[l] > c.halfM[l];
-        decided = true;
-      }
-    }
-    if (gt) {
-      uint32_t b = 0;
-#pragma unroll
-      for (int l = 0; l < kLimbs; ++l) {
-        const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
+      for (int l = 0; l < NL; ++l) {
+        const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
+        qc = qm >> 32;
+        const uint64_t d = static_cast<uint64_t>(x[l]) - static_cast<uint32_t>(qm) - borrow;
         x[l] = static_cast<uint32_t>(d);
-        b = static_cast<uint32_t>(d >> 63);
+        borrow = static_cast<uint32_t>(d >> 63);
       }
-      neg = !neg;
+      bool neg = (x[NL - 1] >> 31) != 0;
+      if (neg) {  // magnitude
+        uint32_t cy = 1;
+#pragma unroll
+        for (int l = 0; l < NL; ++l) {
+          const uint64_t v = static_cast<uint64_t>(~x[l]) + cy;
+          x[l] = static_cast<uint32_t>(v);
+          cy = static_cast<uint32_t>(v >> 32);
+        }
+      }
+      // one correction: if |X| > M/2 the representative is M - |X| with the other sign
+      bool gt = false, decided = false;
+#pragma unroll
+      for (int l = NL - 1; l >= 0; --l) {
+        if (!decided && x[l] != c.halfM[l]) {
+          gt = x[l] > c.halfM[l];
+          decided = true;
+        }
+      }
+      if (gt) {
+        uint32_t b = 0;
+#pragma unroll
+        for (int l = 0; l < NL; ++l) {
+          const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
+          x[l] = static_cast<uint32_t>(d);
+          b = static_cast<uint32_t>(d >> 63);
+        }
+        neg = !neg;
+      }
+#pragma unroll
+      for (int l = NL; l < kLimbs; ++l) x[l] = 0;
+      const int D = 2 * c.kA - E[e] - F;  // d_i + e_j
+      out[e] = __longlong_as_double(static_cast<long long>(round_scaled_bits(x, neg, D)));
     }
-    const int D = 2 * c.kA - E - F;  // d_i + e_j
-    *out = __longlong_as_double(static_cast<long long>(round_scaled_bits(x, neg, D)));
   }
+}
+
+// Limbs needed for Z < 255 s M (host side: bit length of M plus log2(255 s)).
+static int crt_limbs(const CrtConsts& c) {
+  int top = kLimbs - 1;
+  while (top > 0 && c.M[top] == 0) --top;
+  int bits = 32 * top;
+  for (uint32_t v = c.M[top]; v; v >>= 1) ++bits;
+  bits += 13;  // 255 * 20 < 2^13
+  return (bits + 31) / 32;
 }
 
 cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
                        const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
   if (m == 0 || n == 0) return cudaSuccess;
-  dim3 grid((m + 255) / 256, n < 65535 ? n : 65535);
-  crt_kernel<<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  dim3 grid((m + 1023) / 1024, n < 65535 ? n : 65535);
+  const int nl = crt_limbs(c);
+  if (nl <= 3)
+    crt_kernel<3><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  else if (nl == 4)
+    crt_kernel<4><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  else if (nl == 5)
+    crt_kernel<5><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  else
+    crt_kernel<6><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
   return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) rowexp_colmajor_kernel(int m, int k, cons
   const int j1 = min(k, j0 + kRowExpCols);
   const double* p = A + i + static_cast<long long>(j0) * lda;
   int best = OZ_EXP_EMPTY;
-#pragma unroll 8
+#pragma unroll 16
   for (int j = j0; j < j1; ++j, p += lda) best = max(best, ceil_log2_code(__ldg(p)));
   if (best != OZ_EXP_EMPTY) atomicMax(&rowexp[i], best);
 }
@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) colexp_colmajor_kernel(int k, int n, cons
   const int r1 = min(k, r0 + kColExpRows);
   const double* col = B + static_cast<long long>(j) * ldb;
   int best = OZ_EXP_EMPTY;
-#pragma unroll 8
+#pragma unroll 16
   for (int r = r0 + lane; r < r1; r += 32) best = max(best, ceil_log2_code(__ldg(col + r)));
   best = __reduce_max_sync(0xFFFFFFFFu, best);
   if (lane == 0 && best != OZ_EXP_EMPTY) atomicMax(&colexp[j], best);

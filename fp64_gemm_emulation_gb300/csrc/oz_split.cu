@@ -53,14 +53,14 @@ __device__ __forceinline__ uint32_t mod_small(uint32_t y, uint32_t m, uint32_t m
   return y - (__umulhi(y, magic) >> 7) * m;
 }
 
-// Symmetric residue of the packed integer modulo m, in [-(m/2), (m-1)/2].
-__device__ __forceinline__ int sym_residue(uint64_t packed, uint32_t m, uint32_t c16, uint32_t c32,
-                                           uint32_t magic) {
-  const uint64_t u = packed & ((1ull << 53) - 1);
-  const uint32_t p = static_cast<uint32_t>(packed >> 53) & 0x3FFu;
-  const uint32_t x0 = static_cast<uint32_t>(u) & 0xFFFFu;
-  const uint32_t x1 = static_cast<uint32_t>(u) >> 16;
-  const uint32_t x2 = static_cast<uint32_t>(u >> 32);
+// bf16 bit pattern of the symmetric residue of the packed integer modulo m.
+//   r = |a'| mod m                      (16-bit limbs of u, one Barrett step)
+//   w = r, or m - r for a negative a'    (the residue of a' itself, in [1, m])
+//   v = w - m if w >= ceil(m/2) else w   (symmetric representative, [-(m/2), (m-1)/2])
+// and bf16(v) from the float 2^23 + 128 + v (exact), minus 2^23 + 128, top 16 bits:
+// no integer-to-float conversion instruction.
+__device__ __forceinline__ uint32_t residue_bf16(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t p, bool neg,
+                                                 uint32_t m, uint32_t c16, uint32_t c32, uint32_t magic) {
   uint32_t r = mod_small(x2 * c32 + x1 * c16 + x0, m, magic);
   if (p != 0) {
     uint32_t w = 1;
@@ -71,18 +71,10 @@ __device__ __forceinline__ int sym_residue(uint64_t packed, uint32_t m, uint32_t
     r = mod_small(r * w, m, magic);
   }
   const int h = static_cast<int>((m + 1) >> 1);
-  int v = static_cast<int>(r);
-  if (v >= h) v -= static_cast<int>(m);
-  if (packed >> 63) {
-    v = -v;
-    if (v >= h) v -= static_cast<int>(m);
-  }
-  return v;
-}
-
-// bf16 bit pattern of a small integer (|v| <= 256 is exact in bf16).
-__device__ __forceinline__ uint32_t bf16_bits(int v) {
-  return __float_as_uint(static_cast<float>(v)) >> 16;
+  int w = neg ? static_cast<int>(m - r) : static_cast<int>(r);
+  if (w >= h) w -= static_cast<int>(m);
+  const float f = __int_as_float(0x4B000080 + w) - 8388736.0f;  // exactly w
+  return __float_as_uint(f) >> 16;
 }
 
 template <bool kRowsContiguous>
@@ -123,14 +115,27 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
 #pragma unroll
     for (int x = 0; x < 8; ++x) v[x] = tile[g * 8 + x][r];
     uint16_t* dst = planes + static_cast<long long>(r0 + r) * kp + k0 + g * 8;
+    // per element: 16-bit limbs of u, the shift p and the sign, shared by all moduli
+    uint32_t x0[8], x1[8], x2[8], pp[8];
+    bool ng[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint64_t u = v[x] & ((1ull << 53) - 1);
+      x0[x] = static_cast<uint32_t>(u) & 0xFFFFu;
+      x1[x] = static_cast<uint32_t>(u) >> 16;
+      x2[x] = static_cast<uint32_t>(u >> 32);
+      pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
+      ng[x] = (v[x] >> 63) != 0;
+    }
 #pragma unroll 1
     for (int t = 0; t < c.s; ++t) {
       const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
       uint32_t w[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const uint32_t lo = bf16_bits(sym_residue(v[2 * x], m, c16, c32, mg));
-        const uint32_t hi = bf16_bits(sym_residue(v[2 * x + 1], m, c16, c32, mg));
+        const uint32_t lo = residue_bf16(x0[2 * x], x1[2 * x], x2[2 * x], pp[2 * x], ng[2 * x], m, c16, c32, mg);
+        const uint32_t hi =
+            residue_bf16(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], pp[2 * x + 1], ng[2 * x + 1], m, c16, c32, mg);
         w[x] = lo | (hi << 16);
       }
       *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
