@@ -2,13 +2,16 @@
 //
 // [Ozaki II] Algorithm 1, steps 4-6.  Per output element, with residues
 // c_t = C''_t in [0, m_t) and P_t = M_t y_t (< M, so P_t / M = y_t / m_t):
-//   Z    = sum_t c_t P_t                      exact, six 32-bit limbs
-//   Q    = nearest integer to Z / M           from sum_t c_t floor(2^32 y_t / m_t)
-//   C''' = Z - Q M, then one correction by M  symmetric representative, |C'''| < M/2
-//   C    = RN(C''' 2^-(d_i + e_j))            one rounding, subnormals included
-// The quotient estimate errs by less than 1.3e-6, so it is off by at most one and the
-// single correction restores the unique representative ([Ozaki II] section 5: the
-// true product lies in (-M/2, M/2) because 2 c_max < M).  Integer arithmetic only.
+//   Z    = sum_t c_t P_t                      exact, up to six 32-bit limbs
+//   Q    = round(Z / M) or one less            from the top limbs of Z in FP32
+//   X    = Z - Q M, then one correction by M  symmetric representative, |X| < M/2
+//   C    = RN(X 2^-(d_i + e_j))               one rounding, subnormals included
+// The quotient estimate is biased down by 2^-8, more than its error, so it is never
+// too large and at most one too small; one correction then restores the unique
+// representative ([Ozaki II] section 5: the true product lies in (-M/2, M/2) because
+// 2 c_max < M).  The remainder and the rounding are exact integer arithmetic.
+#include <cmath>
+
 #include "oz_internal.h"
 
 namespace oz {
@@ -78,10 +81,56 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLim
   return bits | (neg ? 0x8000000000000000ull : 0ull);
 }
 
+// Fast path of the final rounding for NL-limb magnitudes: the 64 bits below the leading
+// one plus a sticky bit decide RN-even whenever the result is a normal number (or
+// overflows to infinity).  Returns false for results in the subnormal range, which the
+// general routine above handles.
+template <int NL>
+__device__ __forceinline__ bool round_normal_bits(const uint32_t (&x)[kLimbs], bool neg, int D, uint64_t& out) {
+  int h = -1;
+  uint32_t top = 0, nx = 0, nx2 = 0;
+#pragma unroll
+  for (int l = NL - 1; l >= 0; --l) {
+    if (h < 0 && x[l] != 0) {
+      h = l;
+      top = x[l];
+      nx = (l >= 1) ? x[l - 1] : 0u;
+      nx2 = (l >= 2) ? x[l - 2] : 0u;
+    }
+  }
+  if (h < 0) {
+    out = 0;  // exact zero: +0.0
+    return true;
+  }
+  bool sticky = false;
+#pragma unroll
+  for (int l = 0; l < NL; ++l) sticky |= (l <= h - 3) && (x[l] != 0u);
+  const int lz = __clz(top);
+  uint64_t w = (static_cast<uint64_t>(top) << 32 | nx) << lz;
+  if (lz) {
+    w |= nx2 >> (32 - lz);
+    sticky |= (nx2 << lz) != 0u;
+  } else {
+    sticky |= nx2 != 0u;
+  }
+  const int e_unb = (32 * h + 31 - lz) - D;  // exponent of the leading one in the result
+  if (e_unb < -1022) return false;
+  if (e_unb > 1023) {
+    out = 0x7FF0000000000000ull | (neg ? 0x8000000000000000ull : 0ull);
+    return true;
+  }
+  uint64_t mant = w >> 11;
+  const bool rb = (w >> 10) & 1u;
+  sticky |= (w & 0x3FFu) != 0u;
+  if (rb && (sticky || (mant & 1u))) ++mant;  // may carry into 2^53: exponent + 1 below
+  out = ((static_cast<uint64_t>(e_unb + 1022) << 52) + mant) | (neg ? 0x8000000000000000ull : 0ull);
+  return true;
+}
+
 // One thread = 4 consecutive rows i of one column j (a 4-byte load per modulus).
 // NL = 32-bit limbs needed for Z = sum_t c_t P_t (< 255 s M).
 template <int NL>
-__global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c,
+__global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c, float inv_m_top,
                                                   const uint8_t* __restrict__ C_res,
                                                   const int32_t* __restrict__ rowexp,
                                                   const int32_t* __restrict__ colexp, double* __restrict__ C,
@@ -112,20 +161,18 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         out[e] = 0.0;
         continue;
       }
+      // Z = sum_t c_t P_t with 64-bit partial limbs (carries resolved once, below)
       uint64_t acc[NL];
 #pragma unroll
       for (int l = 0; l < NL; ++l) acc[l] = 0;
-      uint64_t qs = 0;
+      const uint32_t sel = 0x4440u | static_cast<uint32_t>(e);
 #pragma unroll
       for (int t = 0; t < kMaxModuli; ++t) {
-        if (t < c.s) {
-          const uint32_t r = (res[t] >> (8 * e)) & 0xFFu;
+        if (t >= c.s) break;
+        const uint32_t r = __byte_perm(res[t], 0u, sel);  // byte e of res[t]
 #pragma unroll
-          for (int l = 0; l < NL; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
-          qs += static_cast<uint64_t>(r) * c.frac[t];
-        }
+        for (int l = 0; l < NL; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
       }
-      // Z in 32-bit limbs
       uint32_t x[kLimbs];
       uint64_t carry = 0;
 #pragma unroll
@@ -134,8 +181,13 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         x[l] = static_cast<uint32_t>(v);
         carry = v >> 32;
       }
-      // X = Z - Q M  (two's complement over NL limbs)
-      const uint32_t Q = static_cast<uint32_t>((qs + 0x80000000ull) >> 32);
+      // Q = floor(Z/M + 1/2 - 2^-8) from the top three limbs in FP32 (error < 2^-9):
+      // round(Z/M) or one less, never more, so X = Z - Q M is the representative or
+      // the representative plus M.
+      float zs = __uint2float_rn(x[NL - 1]);
+      zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, zs);
+      zs = fmaf(__uint2float_rn(x[NL - 3]), 5.421010862427522e-20f, zs);
+      const uint32_t Q = __float2uint_rd(fmaf(zs, inv_m_top, 0.49609375f));
       uint64_t qc = 0;
       uint32_t borrow = 0;
 #pragma unroll
@@ -147,7 +199,7 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         borrow = static_cast<uint32_t>(d >> 63);
       }
       bool neg = (x[NL - 1] >> 31) != 0;
-      if (neg) {  // magnitude
+      if (neg) {  // X is the (negative) representative: take its magnitude
         uint32_t cy = 1;
 #pragma unroll
         for (int l = 0; l < NL; ++l) {
@@ -155,30 +207,32 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
           x[l] = static_cast<uint32_t>(v);
           cy = static_cast<uint32_t>(v >> 32);
         }
-      }
-      // one correction: if |X| > M/2 the representative is M - |X| with the other sign
-      bool gt = false, decided = false;
+      } else {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
+        bool gt = false, decided = false;
 #pragma unroll
-      for (int l = NL - 1; l >= 0; --l) {
-        if (!decided && x[l] != c.halfM[l]) {
-          gt = x[l] > c.halfM[l];
-          decided = true;
+        for (int l = NL - 1; l >= 0; --l) {
+          if (!decided && x[l] != c.halfM[l]) {
+            gt = x[l] > c.halfM[l];
+            decided = true;
+          }
         }
-      }
-      if (gt) {
-        uint32_t b = 0;
+        if (gt) {
+          uint32_t b = 0;
 #pragma unroll
-        for (int l = 0; l < NL; ++l) {
-          const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
-          x[l] = static_cast<uint32_t>(d);
-          b = static_cast<uint32_t>(d >> 63);
+          for (int l = 0; l < NL; ++l) {
+            const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
+            x[l] = static_cast<uint32_t>(d);
+            b = static_cast<uint32_t>(d >> 63);
+          }
+          neg = true;
         }
-        neg = !neg;
       }
 #pragma unroll
       for (int l = NL; l < kLimbs; ++l) x[l] = 0;
       const int D = 2 * c.kA - E[e] - F;  // d_i + e_j
-      out[e] = __longlong_as_double(static_cast<long long>(round_scaled_bits(x, neg, D)));
+      uint64_t bits;
+      if (!round_normal_bits<NL>(x, neg, D, bits)) bits = round_scaled_bits(x, neg, D);
+      out[e] = __longlong_as_double(static_cast<long long>(bits));
     }
   }
 }
@@ -197,15 +251,19 @@ cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const u
                        const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
   if (m == 0 || n == 0) return cudaSuccess;
   dim3 grid((m + 1023) / 1024, n < 65535 ? n : 65535);
-  const int nl = crt_limbs(c);
-  if (nl <= 3)
-    crt_kernel<3><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+  const int nl = crt_limbs(c) < 3 ? 3 : crt_limbs(c);
+  // 2^(32 (nl - 1)) / M: the quotient estimate reads the top limb in units of 2^(32 (nl - 1))
+  double Md = 0.0;
+  for (int l = kLimbs - 1; l >= 0; --l) Md = Md * 4294967296.0 + c.M[l];
+  const float inv_m_top = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / Md);
+  if (nl == 3)
+    crt_kernel<3><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
   else if (nl == 4)
-    crt_kernel<4><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+    crt_kernel<4><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
   else if (nl == 5)
-    crt_kernel<5><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+    crt_kernel<5><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
   else
-    crt_kernel<6><<<grid, 256, 0, stream>>>(m, n, mp, np, c, C_res, rowexp, colexp, C, ldc);
+    crt_kernel<6><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
   return cudaGetLastError();
 }
 

@@ -77,6 +77,20 @@ __device__ __forceinline__ uint32_t residue_bf16(uint32_t x0, uint32_t x1, uint3
   return __float_as_uint(f) >> 16;
 }
 
+// Fast path (p == 0): bf16 bits of the symmetric residue of a' = +-u modulo m.
+//   ys = y, or BIG - y for a negative a' (BIG = m 2^22 > y, a multiple of m)
+//   v  = ys - m floor((ys + floor(m/2)) / m)   -- directly in [-floor(m/2), ceil(m/2) - 1]
+// where y = x2 c32 + x1 c16 + x0 == u (mod m), y < 2^30; ys + floor(m/2) < 2^30.
+__device__ __forceinline__ float residue_fast(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t negmask, uint32_t m,
+                                              uint32_t c16, uint32_t c32, uint32_t magic, uint32_t big,
+                                              uint32_t halfm) {
+  const uint32_t y = x2 * c32 + x1 * c16 + x0;
+  const uint32_t ys = (y ^ negmask) + (big & negmask) + (negmask & 1u);  // y or big - y
+  const uint32_t q = __umulhi(ys + halfm, magic) >> 7;
+  const int v = static_cast<int>(ys - q * m);
+  return __int_as_float(0x4B000080 + v) - 8388736.0f;  // exactly v
+}
+
 template <bool kRowsContiguous>
 __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, const double* __restrict__ X,
                                                               long long rs, long long ks,
@@ -127,18 +141,43 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
       pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
       ng[x] = (v[x] >> 63) != 0;
     }
-#pragma unroll 1
-    for (int t = 0; t < c.s; ++t) {
-      const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-      uint32_t w[4];
+    bool any_p = false;
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const uint32_t lo = residue_bf16(x0[2 * x], x1[2 * x], x2[2 * x], pp[2 * x], ng[2 * x], m, c16, c32, mg);
-        const uint32_t hi =
-            residue_bf16(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], pp[2 * x + 1], ng[2 * x + 1], m, c16, c32, mg);
-        w[x] = lo | (hi << 16);
+    for (int x = 0; x < 8; ++x) any_p |= (pp[x] != 0);
+    if (!__any_sync(0xFFFFFFFFu, any_p)) {
+      // common case: every a' of the warp is u itself (no power-of-two factor)
+      uint32_t nm[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) nm[x] = ng[x] ? 0xFFFFFFFFu : 0u;
+#pragma unroll 1
+      for (int t = 0; t < c.s; ++t) {
+        const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
+        const uint32_t big = m << 22, halfm = m >> 1;
+        uint32_t w[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float lo = residue_fast(x0[2 * x], x1[2 * x], x2[2 * x], nm[2 * x], m, c16, c32, mg, big, halfm);
+          const float hi =
+              residue_fast(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], nm[2 * x + 1], m, c16, c32, mg, big, halfm);
+          w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
+        }
+        *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+#pragma unroll 1
+      for (int t = 0; t < c.s; ++t) {
+        const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
+        uint32_t w[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const uint32_t lo =
+              residue_bf16(x0[2 * x], x1[2 * x], x2[2 * x], pp[2 * x], ng[2 * x], m, c16, c32, mg);
+          const uint32_t hi = residue_bf16(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], pp[2 * x + 1],
+                                           ng[2 * x + 1], m, c16, c32, mg);
+          w[x] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
 }
