@@ -108,9 +108,13 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, int tiles_m, int tiles_n)
   return c;
 }
 
+constexpr int kModeResidue = 0;  // Scheme II: C''_t = (A'_t B'_t) mod m_t, uint8 output
+constexpr int kModeExact = 1;    // Scheme I: exact INT32 slice products
+
+template <int MODE>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmConsts c, uint8_t* __restrict__ C_res, int mp, int np, int nkb) {
+                        const GemmConsts c, void* __restrict__ out_ptr, int mp, int np, int nkb) {
   using namespace gemm;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -130,7 +134,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = mp / BM, tiles_n = np / BN;
   const int units = tiles_m * tiles_n * c.s;
-  const int nchunks = (nkb + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
+  const int kbc = c.kb_per_chunk;
+  const int nchunks = (nkb + kbc - 1) / kbc;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -171,8 +176,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          tma_load_3d(sA + stage * A_STAGE, &tmA, &full[stage], kb * BK, uc.tm * BM, uc.t);
-          tma_load_3d(sB + stage * B_STAGE, &tmB, &full[stage], kb * BK, uc.tn * BN, uc.t);
+          const int pa = (MODE == kModeResidue) ? uc.t : c.a_plane[uc.t];
+          const int pb = (MODE == kModeResidue) ? uc.t : c.b_plane[uc.t];
+          tma_load_3d(sA + stage * A_STAGE, &tmA, &full[stage], kb * BK, uc.tm * BM, pa);
+          tma_load_3d(sB + stage * B_STAGE, &tmB, &full[stage], kb * BK, uc.tn * BN, pb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -206,8 +213,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          const int kb0 = ch * KB_PER_CHUNK;
-          const int kb1 = min(nkb, kb0 + KB_PER_CHUNK);
+          const int kb0 = ch * kbc;
+          const int kb1 = min(nkb, kb0 + kbc);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase)) {
               ok = false;
@@ -220,7 +227,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
               const uint64_t ad = umma_desc_k128(a_addr + kk * UMMA_K * 2);
               const uint64_t bd = umma_desc_k128(b_addr + kk * UMMA_K * 2);
-              const uint32_t accumulate = (ch >= 2 || kb > kb0 || kk > 0) ? 1u : 0u;
+              // residue mode: chunks 2, 3, ... continue on the reduced accumulator;
+              // exact mode: every chunk starts afresh (the epilogue sums them in INT32)
+              const uint32_t accumulate =
+                  ((MODE == kModeResidue && ch >= 2) || kb > kb0 || kk > 0) ? 1u : 0u;
               umma_bf16(d_tmem, ad, bd, IDESC, accumulate);
             }
             umma_commit(&empty[stage]);
@@ -248,6 +258,42 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     const long long plane = static_cast<long long>(np) * mp;
     uint32_t g = 0, eph = 0;
     bool ok = true;
+    if (MODE == kModeExact) {
+      // exact INT32 products: each chunk's exact sum is added into the output tile
+      int32_t* outp = static_cast<int32_t*>(out_ptr);
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        int32_t* base = outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row;
+        for (int ch = 0; ch < nchunks; ++ch, ++g) {
+          const uint32_t acc = g & 1;
+          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+            ok = false;
+            if (lane == 0) record_timeout(abort_flag);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
+#pragma unroll 1
+          for (int cb = 0; cb < 128; cb += 64) {
+            uint32_t v[32], w[32];
+            tmem_ld32(taddr + cb, v);
+            tmem_ld32(taddr + cb + 32, w);
+            tmem_ld_wait();
+            int32_t* o = base + static_cast<long long>(cb) * mp;
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+              int32_t x = __float2int_rn(__uint_as_float(i < 32 ? v[i] : w[i - 32]));  // exact integer
+              if (ch > 0) x += o[static_cast<long long>(i) * mp];
+              o[static_cast<long long>(i) * mp] = x;
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[acc]);
+        }
+      }
+    } else {
+    uint8_t* C_res = static_cast<uint8_t*>(out_ptr);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
       const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
       const float mf = c.modf[uc.t], inv = c.invf[uc.t];
@@ -315,6 +361,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         break;
       }
     }
+    }
   }
 
   tc_fence_before();
@@ -355,14 +402,15 @@ static bool make_plane_map(CUtensorMap* map, const void* base, int s, int rows, 
   return r == CUDA_SUCCESS;
 }
 
-int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
-                        const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream) {
+template <int MODE>
+static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
+                       const uint16_t* A_planes, const uint16_t* B_planes, void* out, cudaStream_t stream) {
   using namespace gemm;
-  if (mp % BM || np % BN || kp % BK) return OZ_EINVAL;
+  if (mp % BM || np % BN || kp % BK || c.kb_per_chunk < 1) return OZ_EINVAL;
   CUtensorMap tmA, tmB;
-  if (!make_plane_map(&tmA, A_planes, c.s, mp, kp, BM)) return OZ_ECUDA;
-  if (!make_plane_map(&tmB, B_planes, c.s, np, kp, BN)) return OZ_ECUDA;
-  if (cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!make_plane_map(&tmA, A_planes, a_planes, mp, kp, BM)) return OZ_ECUDA;
+  if (!make_plane_map(&tmB, B_planes, b_planes, np, kp, BN)) return OZ_ECUDA;
+  if (cudaFuncSetAttribute(residue_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_BYTES)) != cudaSuccess)
     return OZ_ECUDA;
   int dev = 0, sms = 0;
@@ -370,8 +418,20 @@ int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint1
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OZ_ECUDA;
   const long long units = static_cast<long long>(mp / BM) * (np / BN) * c.s;
   const int grid = static_cast<int>(units < sms ? units : sms);
-  residue_gemm_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, c, C_res, mp, np, kp / BK);
+  residue_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, c, out, mp, np, kp / BK);
   return cudaGetLastError() == cudaSuccess ? OZ_OK : OZ_ECUDA;
+}
+
+int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
+                        const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream) {
+  GemmConsts cc = c;
+  cc.kb_per_chunk = gemm::KB_PER_CHUNK;
+  return launch_gemm<kModeResidue>(mp, np, kp, c.s, c.s, cc, A_planes, B_planes, C_res, stream);
+}
+
+int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
+                      const uint16_t* A_planes, const uint16_t* B_planes, int32_t* out, cudaStream_t stream) {
+  return launch_gemm<kModeExact>(mp, np, kp, a_planes, b_planes, c, A_planes, B_planes, out, stream);
 }
 
 }  // namespace oz

@@ -38,11 +38,19 @@ struct CrtConsts {
   uint32_t halfM[kLimbs];          // floor(M / 2)
 };
 
-// Per-modulus constants of the GEMM epilogue (a4).
+constexpr int kMaxPairs = OZ_MAX_SLICES * (OZ_MAX_SLICES + 1) / 2;  // Scheme I products
+
+// Work description of the tcgen05 GEMM engine.  Each work unit is a (tile, product)
+// pair; product p multiplies A plane a_plane[p] by B plane b_plane[p].
+//   residue mode (Scheme II): product t = modulus t, planes t and t, epilogue mod m_t;
+//   exact mode (Scheme I):    product p = slice pair (i, j), exact INT32 output.
 struct GemmConsts {
-  int s;
+  int s;              // number of products
+  int kb_per_chunk;   // k-blocks of 64 whose FP32 sum stays exact
   float modf[kMaxModuli];
   float invf[kMaxModuli];
+  uint8_t a_plane[kMaxPairs];
+  uint8_t b_plane[kMaxPairs];
 };
 
 // Host-side helpers (ozaki_host.cu).
@@ -57,6 +65,8 @@ cudaError_t launch_split(int rows, int k, const double* X, long long row_stride,
                          int kp, cudaStream_t stream);
 int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
                         const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
+int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
+                      const uint16_t* A_planes, const uint16_t* B_planes, int32_t* out, cudaStream_t stream);
 cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
                        const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream);
 cudaError_t launch_fill_zero(int m, int n, double* C, int ldc, cudaStream_t stream);

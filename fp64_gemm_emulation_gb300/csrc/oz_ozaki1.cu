@@ -1,0 +1,375 @@
+// oz_ozaki1.cu -- Ozaki Scheme I: RN split, triangular slice products, FP64 accumulation.
+//
+// [Ozaki notes], RN split of Uchino et al. (step 1: beta = min(7, floor((31 - log2 q)/2));
+// steps 3-7 per slice: mu_i = 2^(ceil(log2 max_j |r_ij|) + 1 - beta),
+// sigma_i = 0.75 * 2^53 * mu_i, S = (r + sigma) - sigma in round-to-nearest, the
+// integer slice S / mu_i, r <- r - S), which is SplitFP's sigma with alpha = beta; then the
+// integer matrix-multiplication algorithm: C = sum over i + j <= s + 1 of
+// diag(mu_A^(i)) (A'_i B'_j) diag(mu_B^(j)), i ascending outside, j ascending inside,
+// each product exact in INT32 and the sum taken in FP64 in that fixed order.
+//
+// GPU mapping:
+//   * rn_split_pass (one launch per slice and operand): reads the residual tile,
+//     rounds it to the slice grid with the same IEEE double operations, writes the
+//     new residual, the slice as a bf16 plane row (K contiguous, exact: |slice| <= 64)
+//     and the row maximum of the new residual for the next pass (atomicMax of
+//     ceil(log2 |.|));
+//   * the slice products run on the tcgen05 engine in exact mode (oz_gemm.cu);
+//   * ozaki1 accumulation: one thread per output element, the s(s+1)/2 exact terms
+//     added in the fixed order with double-precision round-to-nearest additions.
+#include <cmath>
+#include <cstring>
+
+#include "oz_fp.cuh"
+#include "oz_internal.h"
+
+namespace oz {
+
+constexpr int kTile = 64;
+constexpr int kThreads = 256;
+
+// 1.5 * 2^(52 + ex) = 0.75 * 2^53 * 2^ex, the rounding constant of the grid 2^ex.
+__device__ __forceinline__ double sigma_of(int ex) {
+  return __longlong_as_double(static_cast<long long>((static_cast<uint64_t>(1075 + ex) << 52) | (1ull << 51)));
+}
+
+// The integer S / 2^ex of a double S that is an exact multiple of 2^ex with |S / 2^ex| <= 2^52.
+__device__ __forceinline__ int slice_int(double S, int ex) {
+  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(S));
+  const int ef = static_cast<int>((b >> 52) & 0x7FF);
+  if ((b & 0x7FFFFFFFFFFFFFFFull) == 0) return 0;
+  const uint64_t mant = (b & 0x000FFFFFFFFFFFFFull) | (ef ? (1ull << 52) : 0ull);
+  const int e2 = (ef ? ef : 1) - 1075;  // S = mant * 2^e2
+  const int sh = ex - e2;
+  const int64_t v = static_cast<int64_t>(sh >= 0 ? (mant >> sh) : (mant << (-sh)));
+  return static_cast<int>((b >> 63) ? -v : v);
+}
+
+template <bool kRowsContiguous>
+__global__ void __launch_bounds__(kThreads) rn_split_pass_kernel(int rows, int K, const double* Rin,
+                                                                 long long rs_in, long long ks_in, double* Rout,
+                                                                 long long rs_out, long long ks_out,
+                                                                 const int32_t* __restrict__ E, int beta,
+                                                                 uint16_t* __restrict__ plane, int kp,
+                                                                 int32_t* __restrict__ ex_out,
+                                                                 int32_t* __restrict__ E_next) {
+  __shared__ int8_t tile[kTile][kTile + 4];  // [kk][r] slice integers
+  const int tid = threadIdx.x;
+  const int k0 = blockIdx.x * kTile;
+  const int r0 = blockIdx.y * kTile;
+  int local_max = OZ_EXP_EMPTY;
+#pragma unroll 4
+  for (int it = 0; it < (kTile * kTile) / kThreads; ++it) {
+    int r, kk;
+    if (kRowsContiguous) {
+      r = tid & 63;
+      kk = (tid >> 6) + 4 * it;
+    } else {
+      kk = tid & 63;
+      r = (tid >> 6) + 4 * it;
+    }
+    const int gr = r0 + r, gk = k0 + kk;
+    int sl = 0;
+    int code = OZ_EXP_EMPTY;
+    if (gr < rows && gk < K) {
+      const double x = Rin[gr * rs_in + gk * ks_in];
+      const int Er = __ldg(E + gr);
+      double rem = x;
+      if (Er != OZ_EXP_EMPTY) {
+        const int ex = Er + 1 - beta;
+        const double sigma = sigma_of(ex);
+        const double S = __dsub_rn(__dadd_rn(x, sigma), sigma);  // x rounded to the grid 2^ex
+        sl = slice_int(S, ex);
+        rem = __dsub_rn(x, S);                                    // exact
+      }
+      if (Rout) Rout[gr * rs_out + gk * ks_out] = rem;
+      code = ceil_log2_code(rem);
+    }
+    tile[kk][r] = static_cast<int8_t>(sl);
+    if (E_next) {
+      if (kRowsContiguous) {
+        local_max = max(local_max, code);  // same row for all iterations
+      } else {
+        int wmax = __reduce_max_sync(0xFFFFFFFFu, code);  // a warp covers one row
+        if ((tid & 31) == 0 && wmax != OZ_EXP_EMPTY && gr < rows) atomicMax(&E_next[gr], wmax);
+      }
+    }
+  }
+  if (E_next && kRowsContiguous && local_max != OZ_EXP_EMPTY && r0 + (tid & 63) < rows)
+    atomicMax(&E_next[r0 + (tid & 63)], local_max);
+  if (blockIdx.x == 0 && tid < kTile && r0 + tid < rows) {
+    const int Er = E[r0 + tid];
+    ex_out[r0 + tid] = (Er == OZ_EXP_EMPTY) ? 0 : Er + 1 - beta;
+  }
+  __syncthreads();
+  // bf16 plane rows, 8 consecutive k per thread (16-byte stores)
+#pragma unroll 1
+  for (int it = 0; it < (kTile * kTile / 8) / kThreads; ++it) {
+    const int item = tid + kThreads * it;
+    const int g = item & 7, r = item >> 3;
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float lo = __int_as_float(0x4B000080 + tile[g * 8 + 2 * x][r]) - 8388736.0f;
+      const float hi = __int_as_float(0x4B000080 + tile[g * 8 + 2 * x + 1][r]) - 8388736.0f;
+      w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
+    }
+    *reinterpret_cast<uint4*>(plane + static_cast<long long>(r0 + r) * kp + k0 + g * 8) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// C_ij = sum over the triangle, in order, of ldexp(P_p[j][i], exA[ip][i] + exB[jp][j]).
+__global__ void __launch_bounds__(256) ozaki1_accumulate_kernel(int m, int n, int mp, int np, int npairs,
+                                                                const GemmConsts c,
+                                                                const int32_t* __restrict__ prod,
+                                                                const int32_t* __restrict__ exA,
+                                                                const int32_t* __restrict__ exB,
+                                                                double* __restrict__ C, long long ldc) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m) return;
+  const long long plane = static_cast<long long>(np) * mp;
+  for (int j = blockIdx.y; j < n; j += gridDim.y) {
+    double acc = 0.0;
+    const int32_t* p = prod + static_cast<long long>(j) * mp + i;
+#pragma unroll 4
+    for (int q = 0; q < npairs; ++q) {
+      const int v = __ldg(p + q * plane);
+      const int e = __ldg(exA + c.a_plane[q] * m + i) + __ldg(exB + c.b_plane[q] * n + j);
+      acc = __dadd_rn(acc, ldexp(static_cast<double>(v), e));
+    }
+    C[i + j * ldc] = acc;
+  }
+}
+
+}  // namespace oz
+
+using namespace oz;
+
+namespace {
+
+int beta_for(long long k) {
+  // largest b with k * 4^b <= 2^31, capped at 7 (= min(7, floor((31 - log2 k) / 2)))
+  if (k < 1) return -1;
+  int b = 0;
+  while (b < 7 && (static_cast<unsigned long long>(k) << (2 * (b + 1))) <= (1ull << 31)) ++b;
+  if ((static_cast<unsigned long long>(k)) > (1ull << 31)) return -1;
+  return b;
+}
+
+struct Layout1 {
+  int mp, np, kp, npairs;
+  size_t off_RA, off_RB, off_EA, off_EB, scratch_total;  // scratch of the split step
+  size_t off_planesA, off_planesB, off_exA, off_exB, off_prod, off_scratch, total;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout1 layout1(int m, int n, int k, int s) {
+  Layout1 L;
+  L.mp = static_cast<int>(roundup(m, kPadM));
+  L.np = static_cast<int>(roundup(n, kPadN));
+  L.kp = static_cast<int>(roundup(k, kPadK));
+  L.npairs = s * (s + 1) / 2;
+  size_t off = 0;
+  L.off_RA = off;
+  off = a256(off + 8ull * m * k);
+  L.off_RB = off;
+  off = a256(off + 8ull * k * n);
+  L.off_EA = off;  // two row-maximum arrays per operand (current, next)
+  off = a256(off + 8ull * m);
+  L.off_EB = off;
+  off = a256(off + 8ull * n);
+  L.scratch_total = off;
+  off = 0;
+  L.off_planesA = off;
+  off = a256(off + 2ull * s * L.mp * L.kp);
+  L.off_planesB = off;
+  off = a256(off + 2ull * s * L.np * L.kp);
+  L.off_exA = off;
+  off = a256(off + 4ull * s * m);
+  L.off_exB = off;
+  off = a256(off + 4ull * s * n);
+  L.off_prod = off;
+  off = a256(off + 4ull * L.npairs * L.np * L.mp);
+  L.off_scratch = off;
+  off = a256(off + L.scratch_total);
+  L.total = off;
+  return L;
+}
+
+GemmConsts pair_consts(int s, int beta) {
+  GemmConsts g;
+  std::memset(&g, 0, sizeof(g));
+  int q = 0;
+  for (int i = 0; i < s; ++i)
+    for (int j = 0; j + i < s; ++j) {  // (i+1) + (j+1) <= s + 1, i outer, j inner
+      g.a_plane[q] = static_cast<uint8_t>(i);
+      g.b_plane[q] = static_cast<uint8_t>(j);
+      ++q;
+    }
+  g.s = q;
+  // products of slices are <= 2^(2 beta - 2): 2^(26 - 2 beta) of them stay below 2^24
+  const long long chunk_k = 1ll << (26 - 2 * beta);
+  g.kb_per_chunk = static_cast<int>(chunk_k / 64 > 0 ? chunk_k / 64 : 1);
+  return g;
+}
+
+cudaError_t launch_pass(bool rows_contig, int rows, int k, const double* Rin, long long rs_in, long long ks_in,
+                        double* Rout, long long rs_out, long long ks_out, const int32_t* E, int beta,
+                        uint16_t* plane, int rows_padded, int kp, int32_t* ex_out, int32_t* E_next,
+                        cudaStream_t st) {
+  dim3 grid(kp / kTile, rows_padded / kTile);
+  if (rows_contig)
+    rn_split_pass_kernel<true><<<grid, kThreads, 0, st>>>(rows, k, Rin, rs_in, ks_in, Rout, rs_out, ks_out, E, beta,
+                                                          plane, kp, ex_out, E_next);
+  else
+    rn_split_pass_kernel<false><<<grid, kThreads, 0, st>>>(rows, k, Rin, rs_in, ks_in, Rout, rs_out, ks_out, E,
+                                                           beta, plane, kp, ex_out, E_next);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+extern "C" {
+
+int ozaki1_beta(long long k_inner, int* beta_out) {
+  if (!beta_out || k_inner < 1) return OZ_EINVAL;
+  const int b = beta_for(k_inner);
+  if (b < 1) return OZ_ERANGE;
+  *beta_out = b;
+  return OZ_OK;
+}
+
+size_t ozaki1_split_scratch_bytes(int m, int n, int k) {
+  if (m < 0 || n < 0 || k < 0) return 0;
+  return layout1(m, n, k, 1).scratch_total;
+}
+
+size_t ozaki1_workspace_bytes(int m, int n, int k, int num_slices) {
+  if (m < 0 || n < 0 || k < 0 || num_slices < 1 || num_slices > OZ_MAX_SLICES) return 0;
+  return layout1(m, n, k, num_slices).total;
+}
+
+int ozaki1_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_slices,
+                 uint16_t* A_planes, uint16_t* B_planes, int32_t* A_exps, int32_t* B_exps, void* scratch,
+                 size_t scratch_bytes, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || num_slices < 1 || num_slices > OZ_MAX_SLICES) return OZ_EINVAL;
+  if ((A && (lda < (m > 1 ? m : 1) || !A_planes || !A_exps)) || (B && (ldb < (k > 1 ? k : 1) || !B_planes || !B_exps)))
+    return OZ_EINVAL;
+  int beta;
+  int rc = ozaki1_beta(k, &beta);
+  if (rc) return rc;
+  const Layout1 L = layout1(m, n, k, num_slices);
+  if (!scratch || scratch_bytes < L.scratch_total || (reinterpret_cast<uintptr_t>(scratch) & 255)) return OZ_ENOMEM;
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  double* RA = reinterpret_cast<double*>(ws + L.off_RA);
+  double* RB = reinterpret_cast<double*>(ws + L.off_RB);
+  int32_t* EA[2] = {reinterpret_cast<int32_t*>(ws + L.off_EA), reinterpret_cast<int32_t*>(ws + L.off_EA) + m};
+  int32_t* EB[2] = {reinterpret_cast<int32_t*>(ws + L.off_EB), reinterpret_cast<int32_t*>(ws + L.off_EB) + n};
+  // row maxima of the operands themselves
+  if (launch_exponents(m, n, k, A, lda, B, ldb, EA[0], EB[0], stream) != cudaSuccess) return OZ_ECUDA;
+  for (int p = 0; p < num_slices; ++p) {
+    const bool last = (p == num_slices - 1);
+    const int cur = p & 1, nxt = cur ^ 1;
+    if (A && m > 0) {
+      if (!last && cudaMemsetAsync(EA[nxt], 0x80, 4ull * m, stream) != cudaSuccess) return OZ_ECUDA;
+      const double* Rin = p == 0 ? A : RA;
+      const long long ks_in = p == 0 ? lda : m;
+      if (launch_pass(true, m, k, Rin, 1, ks_in, last ? nullptr : RA, 1, m, EA[cur], beta,
+                      A_planes + static_cast<long long>(p) * L.mp * L.kp, L.mp, L.kp, A_exps + static_cast<long long>(p) * m,
+                      last ? nullptr : EA[nxt], stream) != cudaSuccess)
+        return OZ_ECUDA;
+    }
+    if (B && n > 0) {
+      if (!last && cudaMemsetAsync(EB[nxt], 0x80, 4ull * n, stream) != cudaSuccess) return OZ_ECUDA;
+      const double* Rin = p == 0 ? B : RB;
+      const long long rs_in = p == 0 ? ldb : k;
+      if (launch_pass(false, n, k, Rin, rs_in, 1, last ? nullptr : RB, k, 1, EB[cur], beta,
+                      B_planes + static_cast<long long>(p) * L.np * L.kp, L.np, L.kp, B_exps + static_cast<long long>(p) * n,
+                      last ? nullptr : EB[nxt], stream) != cudaSuccess)
+        return OZ_ECUDA;
+    }
+  }
+  return OZ_OK;
+}
+
+int ozaki1_slice_gemm(int m, int n, int k, int num_slices, const uint16_t* A_planes, const uint16_t* B_planes,
+                      int32_t* products, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || num_slices < 1 || num_slices > OZ_MAX_SLICES || !A_planes || !B_planes || !products)
+    return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  int beta;
+  const int rc = ozaki1_beta(k, &beta);
+  if (rc) return rc;
+  const Layout1 L = layout1(m, n, k, num_slices);
+  return launch_slice_gemm(L.mp, L.np, L.kp, num_slices, num_slices, pair_consts(num_slices, beta), A_planes,
+                           B_planes, products, stream);
+}
+
+int ozaki1_accumulate(int m, int n, int k, int num_slices, const int32_t* products, const int32_t* A_exps,
+                      const int32_t* B_exps, double* C, int ldc, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || num_slices < 1 || num_slices > OZ_MAX_SLICES || !products || !A_exps || !B_exps ||
+      !C || ldc < (m > 1 ? m : 1))
+    return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  int beta;
+  const int rc = ozaki1_beta(k, &beta);
+  if (rc) return rc;
+  const Layout1 L = layout1(m, n, k, num_slices);
+  const GemmConsts g = pair_consts(num_slices, beta);
+  dim3 grid((m + 255) / 256, n < 65535 ? n : 65535);
+  ozaki1_accumulate_kernel<<<grid, 256, 0, stream>>>(m, n, L.mp, L.np, g.s, g, products, A_exps, B_exps, C, ldc);
+  return cudaGetLastError() == cudaSuccess ? OZ_OK : OZ_ECUDA;
+}
+
+int ozaki1_dgemm_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                    int num_slices, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || lda < (m > 1 ? m : 1) || ldb < (k > 1 ? k : 1) || ldc < (m > 1 ? m : 1))
+    return OZ_EINVAL;
+  if (num_slices < 1 || num_slices > OZ_MAX_SLICES) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (!C) return OZ_EINVAL;
+  if (k == 0) return launch_fill_zero(m, n, C, ldc, stream) == cudaSuccess ? OZ_OK : OZ_ECUDA;
+  if (!A || !B) return OZ_EINVAL;
+  int beta;
+  int rc = ozaki1_beta(k, &beta);
+  if (rc) return rc;
+  const Layout1 L = layout1(m, n, k, num_slices);
+  if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255)) return OZ_ENOMEM;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + L.off_planesA);
+  uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + L.off_planesB);
+  int32_t* exA = reinterpret_cast<int32_t*>(ws + L.off_exA);
+  int32_t* exB = reinterpret_cast<int32_t*>(ws + L.off_exB);
+  int32_t* prod = reinterpret_cast<int32_t*>(ws + L.off_prod);
+  if ((rc = ozaki1_split(m, n, k, A, lda, B, ldb, num_slices, Ap, Bp, exA, exB, ws + L.off_scratch,
+                         L.scratch_total, stream)))
+    return rc;
+  if ((rc = ozaki1_slice_gemm(m, n, k, num_slices, Ap, Bp, prod, stream))) return rc;
+  return ozaki1_accumulate(m, n, k, num_slices, prod, exA, exB, C, ldc, stream);
+}
+
+int ozaki1_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                 int num_slices, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 0 || lda < (m > 1 ? m : 1) || ldb < (k > 1 ? k : 1) || ldc < (m > 1 ? m : 1))
+    return OZ_EINVAL;
+  if (num_slices < 1 || num_slices > OZ_MAX_SLICES) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (k == 0) return C ? (launch_fill_zero(m, n, C, ldc, stream) == cudaSuccess ? OZ_OK : OZ_ECUDA) : OZ_EINVAL;
+  int beta;
+  int rc = ozaki1_beta(k, &beta);
+  if (rc) return rc;
+  const size_t bytes = ozaki1_workspace_bytes(m, n, k, num_slices);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return OZ_ENOMEM;
+  }
+  rc = ozaki1_dgemm_ws(m, n, k, A, lda, B, ldb, C, ldc, num_slices, ws, bytes, stream);
+  const cudaError_t e = cudaFreeAsync(ws, stream);
+  if (rc == OZ_OK && e != cudaSuccess) rc = OZ_ECUDA;
+  return rc;
+}
+
+}  // extern "C"

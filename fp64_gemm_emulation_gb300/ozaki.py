@@ -50,6 +50,14 @@ def _load():
         "ozaki2_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
         "ozaki2_dgemm_host": (I, [I, I, I, P, I, P, I, P, I, I]),
         "ozaki2_dgemm_noalloc": (I, [I, I, I, P, I, P, I, P, I, I, P]),
+        "ozaki1_beta": (I, [L, P]),
+        "ozaki1_split_scratch_bytes": (S, [I, I, I]),
+        "ozaki1_workspace_bytes": (S, [I, I, I, I]),
+        "ozaki1_split": (I, [I, I, I, P, I, P, I, I, P, P, P, P, P, S, P]),
+        "ozaki1_slice_gemm": (I, [I, I, I, I, P, P, P, P]),
+        "ozaki1_accumulate": (I, [I, I, I, I, P, P, P, P, I, P]),
+        "ozaki1_dgemm_ws": (I, [I, I, I, P, I, P, I, P, I, I, P, S, P]),
+        "ozaki1_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
         "ozaki_get_device_status": (I, []),
         "ozaki_status_string": (ctypes.c_char_p, [I]),
     }
@@ -223,6 +231,87 @@ def ozaki2_dgemm_host(A: np.ndarray, B: np.ndarray, num_moduli: int = 14, C: np.
 def ozaki2_dgemm_host_ptr(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli):
     """Raw-pointer form of ozaki2_dgemm_host (host pointers, e.g. pinned torch tensors)."""
     _check(_lib.ozaki2_dgemm_host(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli), "ozaki2_dgemm_host")
+
+
+# ------------------------------------------------------------------ Scheme I
+def ozaki1_beta(k_inner: int) -> int:
+    b = ctypes.c_int()
+    _check(_lib.ozaki1_beta(k_inner, ctypes.byref(b)), "ozaki1_beta")
+    return b.value
+
+
+def ozaki1_split_scratch_bytes(m: int, n: int, k: int) -> int:
+    return int(_lib.ozaki1_split_scratch_bytes(m, n, k))
+
+
+def ozaki1_workspace_bytes(m: int, n: int, k: int, num_slices: int) -> int:
+    return int(_lib.ozaki1_workspace_bytes(m, n, k, num_slices))
+
+
+def ozaki1_split(A, B, num_slices: int, stream=None):
+    """RN split: (A_planes [s,Mp,Kp], B_planes [s,Np,Kp] as int16 bf16 bits, A_exps [s,m], B_exps [s,n])."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    Ap = torch.empty((num_slices, mp, kp), dtype=torch.int16, device=A.device)
+    Bp = torch.empty((num_slices, np_, kp), dtype=torch.int16, device=A.device)
+    Ae = torch.empty((num_slices, m), dtype=torch.int32, device=A.device)
+    Be = torch.empty((num_slices, n), dtype=torch.int32, device=A.device)
+    nbytes = ozaki1_split_scratch_bytes(m, n, k)
+    scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=A.device)
+    sp = (scratch.data_ptr() + 255) // 256 * 256
+    _check(_lib.ozaki1_split(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_slices, _ptr(Ap), _ptr(Bp),
+                             _ptr(Ae), _ptr(Be), sp, nbytes, _stream(stream)), "ozaki1_split")
+    return Ap, Bp, Ae, Be
+
+
+def ozaki1_slice_gemm(m: int, n: int, k: int, num_slices: int, A_planes, B_planes, stream=None):
+    """Exact INT32 products [s(s+1)/2, Np, Mp] of the slice pairs (i outer, j inner)."""
+    import torch
+
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    P = torch.empty((num_slices * (num_slices + 1) // 2, np_, mp), dtype=torch.int32, device=A_planes.device)
+    _check(_lib.ozaki1_slice_gemm(m, n, k, num_slices, _ptr(A_planes), _ptr(B_planes), _ptr(P), _stream(stream)),
+           "ozaki1_slice_gemm")
+    return P
+
+
+def ozaki1_accumulate(m: int, n: int, k: int, num_slices: int, products, A_exps, B_exps, C=None, stream=None):
+    import torch
+
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=products.device).t()
+    _check(_lib.ozaki1_accumulate(m, n, k, num_slices, _ptr(products), _ptr(A_exps), _ptr(B_exps), _ptr(C), _ld(C),
+                                  _stream(stream)), "ozaki1_accumulate")
+    return C
+
+
+def ozaki1_dgemm(A, B, num_slices: int = 7, C=None, stream=None):
+    """C = A B by Ozaki Scheme I (stream-ordered workspace inside the library)."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    _check(_lib.ozaki1_dgemm(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_slices,
+                             _stream(stream)), "ozaki1_dgemm")
+    return C
+
+
+def ozaki1_dgemm_ws(A, B, num_slices: int, workspace, C=None, stream=None):
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    _check(_lib.ozaki1_dgemm_ws(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_slices,
+                                _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ozaki1_dgemm_ws")
+    return C
 
 
 def ozaki_get_device_status() -> int:

@@ -134,6 +134,55 @@ int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
 int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                       double* C, int ldc, int num_moduli);
 
+/* ---------------------------------------------------------------- Scheme I (comparison path) */
+
+/* Scheme I ([Ozaki notes]: RN split of Uchino et al., the triangular integer products
+ * i + j <= s + 1, FP64 accumulation).  Layout of its intermediates:
+ *  - A_planes [s][Mp][Kp], B_planes [s][Np][Kp]: bf16 bit patterns of the integer slices
+ *    (|slice| <= 2^(beta-1) <= 64, exact in bf16), same orientation as Scheme II's planes;
+ *  - A_exps [s][m], B_exps [s][n] (int32): slice p of row i of A is
+ *    A_planes[p][i][:] * 2^A_exps[p][i] (0 for rows that are zero at that slice);
+ *  - products [s(s+1)/2][Np][Mp] (int32, column-major per product): the exact product
+ *    A'_i B'_j for the pairs (i, j) in the order i = 1..s outside, j = 1..s-i+1 inside.
+ * Supported inputs: finite, with every row maximum of A and column maximum of B in
+ * [2^-1000, 2^960] or zero (the rounding constants 0.75 * 2^53 * mu must be finite and mu
+ * normal). */
+
+/* beta = min(7, floor((31 - log2 k_inner) / 2)) ([Ozaki notes], RN split step 1):
+ * slice width in bits.  OZ_ERANGE if beta < 1.  No GPU needed. */
+int ozaki1_beta(long long k_inner, int* beta_out);
+
+/* Device scratch ozaki1_split needs for the residuals and row maxima. */
+size_t ozaki1_split_scratch_bytes(int m, int n, int k);
+
+/* Bytes of device workspace ozaki1_dgemm_ws needs (0 on invalid arguments). */
+size_t ozaki1_workspace_bytes(int m, int n, int k, int num_slices);
+
+/* RN split of the rows of A and the columns of B into num_slices (1..OZ_MAX_SLICES)
+ * integer slices each (remainder dropped): planes and slice exponents as above.  Either
+ * operand may be skipped with NULL.  scratch: device memory of at least
+ * ozaki1_split_scratch_bytes(m, n, k) bytes, 256-byte aligned. */
+int ozaki1_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_slices,
+                 uint16_t* A_planes, uint16_t* B_planes, int32_t* A_exps, int32_t* B_exps,
+                 void* scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* The s(s+1)/2 exact integer products A'_i B'_j (tensor cores, INT32 output). */
+int ozaki1_slice_gemm(int m, int n, int k, int num_slices, const uint16_t* A_planes,
+                      const uint16_t* B_planes, int32_t* products, cudaStream_t stream);
+
+/* C = sum over the pairs, in order, of diag(2^A_exps[i]) P_ij diag(2^B_exps[j]), every term
+ * exact, accumulated with FP64 round-to-nearest additions starting from +0. */
+int ozaki1_accumulate(int m, int n, int k, int num_slices, const int32_t* products,
+                      const int32_t* A_exps, const int32_t* B_exps, double* C, int ldc,
+                      cudaStream_t stream);
+
+/* C = A*B by Scheme I with a caller-owned workspace / with a stream-ordered one. */
+int ozaki1_dgemm_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    double* C, int ldc, int num_slices, void* workspace, size_t ws_bytes,
+                    cudaStream_t stream);
+int ozaki1_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                 double* C, int ldc, int num_slices, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- without allocation */
 
 /* Size of the fixed scratch buffer ozaki2_dgemm_noalloc uses (64 MiB). */

@@ -96,3 +96,26 @@ def test_binding_names_follow_the_header(oz):
     for name in declared_functions():
         if name.startswith("ozaki"):
             assert hasattr(oz, name), name
+
+
+@pytest.mark.parametrize("q", [1, 2, 3, 255, 256, 4095, 4096, 4097, 16384, 65536, 2**17, 2**17 + 1,
+                               262144, 2**20, 2**25, 2**29])
+def test_ozaki1_beta_matches_the_oracle(oz, q):
+    from oracle import ozaki1 as O1
+
+    want = O1.beta_rn(q)
+    if want < 1:
+        with pytest.raises(oz.OzakiError):
+            oz.ozaki1_beta(q)
+    else:
+        assert oz.ozaki1_beta(q) == want
+
+
+def test_ozaki1_workspace(oz):
+    s = 7
+    ws = oz.ozaki1_workspace_bytes(300, 520, 2100, s)
+    mp, np_, kp = oz.ozaki2_plane_dims(300, 520, 2100)
+    assert ws >= 2 * s * (mp + np_) * kp + 4 * (s * (s + 1) // 2) * mp * np_
+    assert oz.ozaki1_workspace_bytes(300, 520, 2100, 0) == 0
+    assert oz.ozaki1_workspace_bytes(300, 520, 2100, 21) == 0
+    assert oz.ozaki1_split_scratch_bytes(300, 520, 2100) >= 8 * (300 * 2100 + 2100 * 520)
