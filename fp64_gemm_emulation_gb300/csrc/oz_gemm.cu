@@ -30,23 +30,28 @@
 namespace oz {
 
 namespace gemm {
-constexpr int BM = 128;
-constexpr int BN = 256;
+// A CTA pair computes a 256 x 256 tile: each CTA holds 128 rows of A and 128 rows (the
+// N dimension) of B per stage, and its 128 rows of the accumulator in its own TMEM.
+constexpr int BM = 256;          // tile rows (both CTAs)
+constexpr int BN = 256;          // tile columns
+constexpr int HALF_M = BM / 2;   // rows per CTA
+constexpr int HALF_N = BN / 2;   // B rows per CTA
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int KB_PER_CHUNK = 15;  // 960 k per exactly-representable chunk
-constexpr uint32_t A_STAGE = BM * BK * 2;
-constexpr uint32_t B_STAGE = BN * BK * 2;
+constexpr uint32_t A_STAGE = HALF_M * BK * 2;
+constexpr uint32_t B_STAGE = HALF_N * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int EPI_WARPS = 8;                 // two per SM sub-partition
 constexpr int EPI_THREADS = EPI_WARPS * 32;
 constexpr int THREADS = 64 + EPI_THREADS;   // TMA warp, MMA warp, epilogue warps
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t STASH_BYTES = BM * BN;   // one uint8 residue tile, [col][row]
+constexpr uint32_t TMEM_COLS = 512;         // two 128-lane x 256-column FP32 accumulators
+constexpr uint32_t STASH_BYTES = HALF_M * BN;  // this CTA's uint8 residue half tile, [col][row]
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + STASH_BYTES + 256 /*barriers*/;
 constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
 static_assert(255 + KB_PER_CHUNK * BK * 128 * 128 <= (1 << 24), "chunk too long for exact FP32 sums");
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 }  // namespace gemm
 
 __device__ int g_status = 0;
@@ -120,18 +125,21 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  uint8_t* stash = smem + STAGES * STAGE_BYTES;  // [BN][BM] uint8 residues
+  uint8_t* stash = smem + STAGES * STAGE_BYTES;  // [128 cols][128 rows]... see epilogue
   uint64_t* bars = reinterpret_cast<uint64_t*>(stash + STASH_BYTES);
-  uint64_t* full = bars;                  // [STAGES]  TMA -> MMA
-  uint64_t* empty = bars + STAGES;        // [STAGES]  MMA -> TMA
-  uint64_t* accfull = bars + 2 * STAGES;  // [2]       MMA -> epilogue
-  uint64_t* accempty = accfull + 2;       // [2]       epilogue -> MMA
-  uint64_t* drain = accempty + 2;         // [1]       MMA drain on the error path
-  uint64_t* epibar = drain + 1;           // [1]       epilogue warps rendezvous
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epibar + 1);
+  uint64_t* full = bars;                  // [STAGES]  TMA (both CTAs) -> MMA   (used in the leader)
+  uint64_t* empty = bars + STAGES;        // [STAGES]  MMA -> TMA               (both CTAs)
+  uint64_t* accfull = bars + 2 * STAGES;  // [2]       MMA -> epilogue          (both CTAs)
+  uint64_t* accempty = accfull + 2;       // [2]       epilogues (both) -> MMA  (used in the leader)
+  uint64_t* drain = accempty + 2;         // [1]       all MMAs of the pair done (both CTAs)
+  uint64_t* epibar = drain + 1;           // [1]       epilogue warps rendezvous (per CTA)
+  uint64_t* exitbar = epibar + 1;         // [1]       the peer has finished (per CTA)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exitbar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();      // 0 = leader of the pair, 1 = peer
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int tiles_m = mp / BM, tiles_n = np / BN;
   const int units = tiles_m * tiles_n * c.s;
   const int kbc = c.kb_per_chunk;
@@ -139,47 +147,51 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], 2);  // one arrival (with its bytes) from each CTA's producer
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], EPI_WARPS);
+      mbar_init(&accempty[i], 2 * EPI_WARPS);  // every epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
     mbar_init(epibar, EPI_WARPS);
+    mbar_init(exitbar, 1);
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // barrier initialisation visible to the peer before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
+      // ------------------------------------------------------------ TMA producer (both CTAs)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+      for (int u = pair; u < units && !*abort_flag; u += npairs) {
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        const int pa = (MODE == kModeResidue) ? uc.t : c.a_plane[uc.t];
+        const int pb = (MODE == kModeResidue) ? uc.t : c.b_plane[uc.t];
+        const int rowA = uc.tm * BM + static_cast<int>(rank) * HALF_M;
+        const int rowB = uc.tn * BN + static_cast<int>(rank) * HALF_N;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             record_timeout(abort_flag);
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          const int pa = (MODE == kModeResidue) ? uc.t : c.a_plane[uc.t];
-          const int pb = (MODE == kModeResidue) ? uc.t : c.b_plane[uc.t];
-          tma_load_3d(sA + stage * A_STAGE, &tmA, &full[stage], kb * BK, uc.tm * BM, pa);
-          tma_load_3d(sB + stage * B_STAGE, &tmB, &full[stage], kb * BK, uc.tn * BN, pb);
+          const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          mbar_arrive_expect_tx_cluster(full_leader, STAGE_BYTES);
+          tma_load_3d_pair(sA + stage * A_STAGE, &tmA, full_leader, kb * BK, rowA, pa);
+          tma_load_3d_pair(sB + stage * B_STAGE, &tmB, full_leader, kb * BK, rowB, pb);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -187,24 +199,26 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
         }
       }
-      // Every issued copy must land before the CTA may exit: wait for the last
-      // (up to STAGES) of them.  On the normal path these completed long ago.
+      // Every issued copy must have landed before the pair may exit; the MMA thread has
+      // consumed them on the normal path.  The copies complete on the leader's barriers,
+      // which the leader's MMA thread drains (below); here wait for this CTA's stages to
+      // be released by the MMAs that read them.
       for (int i = 0; i < STAGES && i < issued; ++i) {
         if (--stage < 0) {
           stage = STAGES - 1;
           phase ^= 1;
         }
-        if (!mbar_wait(&full[stage], phase)) record_timeout(abort_flag);
+        if (!mbar_wait(&empty[stage], phase)) record_timeout(abort_flag);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------------ MMA issuer (leader only)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t g = 0;  // chunk counter: accumulator g & 1
       bool ok = true;
-      for (int u = blockIdx.x; u < units && ok && !*abort_flag; u += gridDim.x) {
+      for (int u = pair; u < units && ok && !*abort_flag; u += npairs) {
         for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
           const uint32_t acc = g & 1;
           if (!mbar_wait(&accempty[acc], ((g >> 1) & 1) ^ 1)) {
@@ -231,39 +245,39 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
               // exact mode: every chunk starts afresh (the epilogue sums them in INT32)
               const uint32_t accumulate =
                   ((MODE == kModeResidue && ch >= 2) || kb > kb0 || kk > 0) ? 1u : 0u;
-              umma_bf16(d_tmem, ad, bd, IDESC, accumulate);
+              umma_bf16_pair(d_tmem, ad, bd, IDESC, accumulate);
             }
-            umma_commit(&empty[stage]);
+            umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1;
             }
           }
           if (!ok) break;
-          umma_commit(&accfull[acc]);
+          umma_commit_pair(&accfull[acc], 0x3);  // the chunk is in both CTAs' TMEM
         }
       }
       if (!ok) record_timeout(abort_flag);
-      // Make sure no MMA is still writing tensor memory before it is released.
-      umma_commit(drain);
-      if (!mbar_wait(drain, 0)) record_timeout(abort_flag);
+      umma_commit_pair(drain, 0x3);  // arrives in both CTAs once every MMA above is done
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2-9)
-    // Thread = one accumulator row (TMEM lane) and one half of the 256 columns.
+    // ------------------------------------------------------------ epilogue (warps 2-9, both CTAs)
+    // Thread = one accumulator row (TMEM lane) of this CTA's 128 rows and one half of the
+    // 256 columns.
     const int quad = warp & 3;             // TMEM lanes 32*quad .. 32*quad+31
     const int half = (warp - 2) >> 2;      // columns [128*half, 128*half + 128)
     const int row = quad * 32 + lane;
     const int etid = threadIdx.x - 64;     // 0 .. EPI_THREADS-1
     const long long plane = static_cast<long long>(np) * mp;
+    const int row_off = static_cast<int>(rank) * HALF_M;  // this CTA's rows of the tile
     uint32_t g = 0, eph = 0;
     bool ok = true;
     if (MODE == kModeExact) {
-      // exact INT32 products: each chunk's exact sum is added into the output tile
       int32_t* outp = static_cast<int32_t*>(out_ptr);
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int u = pair; u < units && ok; u += npairs) {
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
-        int32_t* base = outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row;
+        int32_t* base =
+            outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row_off + row;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
           if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
@@ -289,85 +303,94 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[acc]);
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
         }
       }
     } else {
-    uint8_t* C_res = static_cast<uint8_t*>(out_ptr);
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
-      const float mf = c.modf[uc.t], inv = c.invf[uc.t];
-      const uint32_t mi = static_cast<uint32_t>(mf);
-      for (int ch = 0; ch < nchunks; ++ch, ++g) {
-        const uint32_t acc = g & 1;
-        if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
-          ok = false;
+      uint8_t* C_res = static_cast<uint8_t*>(out_ptr);
+      for (int u = pair; u < units && ok; u += npairs) {
+        const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        const float mf = c.modf[uc.t], inv = c.invf[uc.t];
+        const uint32_t mi = static_cast<uint32_t>(mf);
+        for (int ch = 0; ch < nchunks; ++ch, ++g) {
+          const uint32_t acc = g & 1;
+          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+            ok = false;
+            if (lane == 0) record_timeout(abort_flag);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
+          const bool final_chunk = (ch + 2 >= nchunks);
+          const bool combine = final_chunk && (ch == nchunks - 1) && (nchunks >= 2);
+#pragma unroll 1
+          for (int cb = 0; cb < 128; cb += 64) {
+            uint32_t v[32], w[32];
+            tmem_ld32(taddr + cb, v);
+            tmem_ld32(taddr + cb + 32, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
+              w[i] = __float_as_uint(exact_mod(__uint_as_float(w[i]), mf, inv));
+            }
+            if (!final_chunk) {
+              tmem_st32(taddr + cb, v);
+              tmem_st32(taddr + cb + 32, w);
+            } else {
+              uint8_t* col0 = stash + (half * 128 + cb) * HALF_M + row;  // [col][row]
+#pragma unroll
+              for (int i = 0; i < 64; ++i) {
+                uint32_t r = small_float_to_u8(__uint_as_float(i < 32 ? v[i] : w[i - 32]));
+                if (combine) {
+                  r += col0[i * HALF_M];
+                  r = (r >= mi) ? r - mi : r;
+                }
+                col0[i * HALF_M] = static_cast<uint8_t>(r);
+              }
+            }
+          }
+          if (!final_chunk) tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
+        }
+        if (!ok) break;
+        // The finished half tile (128 rows x 256 columns) is in the stash: copy it out with
+        // coalesced 16-byte stores (column j of this half is 128 contiguous bytes of plane t).
+        if (!epilogue_sync(epibar, eph)) {
           if (lane == 0) record_timeout(abort_flag);
           break;
         }
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
-        const bool final_chunk = (ch + 2 >= nchunks);
-        const bool combine = final_chunk && (ch == nchunks - 1) && (nchunks >= 2);
-#pragma unroll 1
-        for (int cb = 0; cb < 128; cb += 64) {
-          uint32_t v[32], w[32];
-          tmem_ld32(taddr + cb, v);
-          tmem_ld32(taddr + cb + 32, w);
-          tmem_ld_wait();
+        uint8_t* dst = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM + row_off;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
-            w[i] = __float_as_uint(exact_mod(__uint_as_float(w[i]), mf, inv));
-          }
-          if (!final_chunk) {
-            tmem_st32(taddr + cb, v);
-            tmem_st32(taddr + cb + 32, w);
-          } else {
-            uint8_t* col0 = stash + (half * 128 + cb) * BM + row;  // [col][row]
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-              uint32_t r = small_float_to_u8(__uint_as_float(i < 32 ? v[i] : w[i - 32]));
-              if (combine) {
-                r += col0[i * BM];
-                r = (r >= mi) ? r - mi : r;
-              }
-              col0[i * BM] = static_cast<uint8_t>(r);
-            }
-          }
+        for (int i = 0; i < (BN * HALF_M / 16) / EPI_THREADS; ++i) {
+          const int q = etid + i * EPI_THREADS;
+          const int col = q >> 3, part = q & 7;
+          *reinterpret_cast<uint4*>(dst + static_cast<long long>(col) * mp + part * 16) =
+              *reinterpret_cast<const uint4*>(stash + col * HALF_M + part * 16);
         }
-        if (!final_chunk) tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[acc]);
+        if (!epilogue_sync(epibar, eph)) {
+          if (lane == 0) record_timeout(abort_flag);
+          break;
+        }
       }
-      if (!ok) break;
-      // The finished tile is in the stash: copy it out with coalesced 16-byte stores
-      // (column j of the tile is 128 contiguous bytes of plane t).
-      if (!epilogue_sync(epibar, eph)) {
-        if (lane == 0) record_timeout(abort_flag);
-        break;
-      }
-      uint8_t* dst = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM;
-#pragma unroll
-      for (int i = 0; i < (BN * BM / 16) / EPI_THREADS; ++i) {
-        const int q = etid + i * EPI_THREADS;
-        const int col = q >> 3, part = q & 7;
-        *reinterpret_cast<uint4*>(dst + static_cast<long long>(col) * mp + part * 16) =
-            *reinterpret_cast<const uint4*>(stash + col * BM + part * 16);
-      }
-      if (!epilogue_sync(epibar, eph)) {
-        if (lane == 0) record_timeout(abort_flag);
-        break;
-      }
-    }
     }
   }
 
+  // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    // every MMA of the pair (and every commit before it) has completed ...
+    if (!mbar_wait(drain, 0)) record_timeout(abort_flag);
+    // ... and the peer is done with this CTA's barriers and shared memory
+    mbar_arrive_cluster(mapa_shared(smem_u32(exitbar), rank ^ 1u));
+    if (!mbar_wait(exitbar, 0)) record_timeout(abort_flag);
+  }
+  __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, gemm::TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ host side
@@ -408,8 +431,8 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   using namespace gemm;
   if (mp % BM || np % BN || kp % BK || c.kb_per_chunk < 1) return OZ_EINVAL;
   CUtensorMap tmA, tmB;
-  if (!make_plane_map(&tmA, A_planes, a_planes, mp, kp, BM)) return OZ_ECUDA;
-  if (!make_plane_map(&tmB, B_planes, b_planes, np, kp, BN)) return OZ_ECUDA;
+  if (!make_plane_map(&tmA, A_planes, a_planes, mp, kp, HALF_M)) return OZ_ECUDA;
+  if (!make_plane_map(&tmB, B_planes, b_planes, np, kp, HALF_N)) return OZ_ECUDA;
   if (cudaFuncSetAttribute(residue_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(SMEM_BYTES)) != cudaSuccess)
     return OZ_ECUDA;
@@ -417,8 +440,21 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OZ_ECUDA;
   const long long units = static_cast<long long>(mp / BM) * (np / BN) * c.s;
-  const int grid = static_cast<int>(units < sms ? units : sms);
-  residue_gemm_kernel<MODE><<<grid, THREADS, SMEM_BYTES, stream>>>(tmA, tmB, c, out, mp, np, kp / BK);
+  const int pairs = static_cast<int>(units < sms / 2 ? units : sms / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int nkb = kp / BK;
+  if (cudaLaunchKernelEx(&cfg, residue_gemm_kernel<MODE>, tmA, tmB, c, out, mp, np, nkb) != cudaSuccess) return OZ_ECUDA;
   return cudaGetLastError() == cudaSuccess ? OZ_OK : OZ_ECUDA;
 }
 
