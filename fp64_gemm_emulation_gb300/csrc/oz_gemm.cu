@@ -5,21 +5,24 @@
 // MMA, so the same exact products run on the BF16 tensor-core path: every residue in
 // [-128, 127] is exact in bf16, every product (<= 2^14) is exact, and the FP32
 // accumulator in tensor memory adds integers exactly while |partial sum| <= 2^24.
-// The k loop is therefore cut into chunks of 960 (= 15 stages of 64):
-//     255 + 960 * 2^14 < 2^24,
-// and after each chunk the epilogue warps reduce the accumulator mod m_t in place
-// (tcgen05.ld -> exact float remainder -> tcgen05.st), so the next chunk accumulates
-// on a value in [0, m_t).  Two accumulators alternate so the tensor cores keep
-// running while one is being reduced.  The last two chunks of a tile are not written
-// back: the first one's residues are kept in a shared-memory tile, the second one's are
-// added to them mod m_t, and the finished uint8 tile leaves with coalesced 16-byte stores.
-// This replaces the pages' block multiplication for k >= 2^17: the result is exact
-// for every k.
+// The k loop is therefore cut into chunks of 1024 (1024 * 2^14 = 2^24).  Each chunk
+// starts from zero in one of two alternating TMEM accumulators; the epilogue warps read
+// it (tcgen05.ld), hand the accumulator straight back to the MMA, reduce the 32 values
+// of each load exactly mod m_t in FP32 and add them, mod m_t, to running residues held
+// in registers (two 16-bit lanes per register).  After the tile's last chunk the
+// residues go through shared memory to coalesced 16-byte stores of the uint8 plane.
+// This replaces the pages' block multiplication for k >= 2^17: the result is exact for
+// every k.  The same engine in exact mode (Scheme I) converts each chunk to INT32 and
+// adds it into the output.
 //
-// Kernel shape (one CTA per SM, persistent over work units (tile, modulus)):
-//   tile 128 x 256 (UMMA M=128, N=256, K=16), stage = 64 k (128-byte rows, 128B swizzle)
-//   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer   warps 2-9: epilogue
-//   TMEM: 512 columns = two 128 x 256 FP32 accumulators.
+// Kernel shape: clusters of two CTAs (cta_group::2), persistent over work units
+// (256 x 256 tile, modulus).  Each CTA loads its 128 rows of A and its 128 rows of B
+// per 64-k stage (TMA, 128-byte swizzle, 6 stages of 32 KB) completing on the pair
+// leader's mbarrier; the leader issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16)
+// and multicasts its commits to both CTAs; each CTA's epilogue drains its own 128
+// TMEM lanes.
+//   warp 0: TMA producer   warp 1: TMEM owner + MMA issuer (leader)   warps 2-9: epilogue
+//   TMEM: 512 columns per CTA = two 128-lane x 256-column FP32 accumulators.
 // Every mbarrier wait is bounded (oz::mbar_wait); on expiry the CTA records
 // OZ_ETIMEOUT in the device status word, drains what it issued and returns.
 #include <cuda.h>
@@ -39,7 +42,7 @@ constexpr int HALF_N = BN / 2;   // B rows per CTA
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int STAGES = 6;
-constexpr int KB_PER_CHUNK = 15;  // 960 k per exactly-representable chunk
+constexpr int KB_PER_CHUNK = 16;  // 1024 k per chunk: |sum| <= 1024 * 2^14 = 2^24, exact in FP32
 constexpr uint32_t A_STAGE = HALF_M * BK * 2;
 constexpr uint32_t B_STAGE = HALF_N * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
@@ -50,7 +53,7 @@ constexpr uint32_t TMEM_COLS = 512;         // two 128-lane x 256-column FP32 ac
 constexpr uint32_t STASH_BYTES = HALF_M * BN;  // this CTA's uint8 residue half tile, [col][row]
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + STASH_BYTES + 256 /*barriers*/;
 constexpr uint32_t IDESC = umma_idesc_bf16_f32(BM, BN);
-static_assert(255 + KB_PER_CHUNK * BK * 128 * 128 <= (1 << 24), "chunk too long for exact FP32 sums");
+static_assert(KB_PER_CHUNK * BK * 128 * 128 <= (1 << 24), "chunk too long for exact FP32 sums");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 }  // namespace gemm
 
@@ -74,11 +77,6 @@ __device__ __forceinline__ float exact_mod(float v, float m, float inv_m) {
   const float q = fmaf(v, inv_m, 12582912.0f) - 12582912.0f;
   const float r = fmaf(-q, m, v);
   return r < 0.0f ? r + m : r;
-}
-
-// Low 8 bits of a float holding an integer in [0, 256).
-__device__ __forceinline__ uint32_t small_float_to_u8(float r) {
-  return __float_as_uint(r + 8388608.0f) & 0xFFu;
 }
 
 // Rendezvous of the epilogue warps on an mbarrier (one arrival per warp), with the same
@@ -241,10 +239,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
               const uint64_t ad = umma_desc_k128(a_addr + kk * UMMA_K * 2);
               const uint64_t bd = umma_desc_k128(b_addr + kk * UMMA_K * 2);
-              // residue mode: chunks 2, 3, ... continue on the reduced accumulator;
-              // exact mode: every chunk starts afresh (the epilogue sums them in INT32)
-              const uint32_t accumulate =
-                  ((MODE == kModeResidue && ch >= 2) || kb > kb0 || kk > 0) ? 1u : 0u;
+              // every chunk starts afresh; the epilogue combines the chunks (mod m_t in
+              // residue mode, exactly in INT32 in exact mode)
+              const uint32_t accumulate = (kb > kb0 || kk > 0) ? 1u : 0u;
               umma_bf16_pair(d_tmem, ad, bd, IDESC, accumulate);
             }
             umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
@@ -311,7 +308,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       for (int u = pair; u < units && ok; u += npairs) {
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         const float mf = c.modf[uc.t], inv = c.invf[uc.t];
-        const uint32_t mi = static_cast<uint32_t>(mf);
+        const uint32_t mm2 = static_cast<uint32_t>(mf) * 0x10001u;  // m in both 16-bit halves
+        // running residues of this thread's 128 columns, two per register (16-bit lanes)
+        uint32_t run[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) run[i] = 0;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
           if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
@@ -321,43 +322,37 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
-          const bool final_chunk = (ch + 2 >= nchunks);
-          const bool combine = final_chunk && (ch == nchunks - 1) && (nchunks >= 2);
-#pragma unroll 1
-          for (int cb = 0; cb < 128; cb += 64) {
-            uint32_t v[32], w[32];
-            tmem_ld32(taddr + cb, v);
-            tmem_ld32(taddr + cb + 32, w);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t v[32];
+            tmem_ld32(taddr + cb * 32, v);
             tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              v[i] = __float_as_uint(exact_mod(__uint_as_float(v[i]), mf, inv));
-              w[i] = __float_as_uint(exact_mod(__uint_as_float(w[i]), mf, inv));
+            if (cb == 3) {  // the whole chunk is in registers: hand the accumulator back
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
             }
-            if (!final_chunk) {
-              tmem_st32(taddr + cb, v);
-              tmem_st32(taddr + cb + 32, w);
-            } else {
-              uint8_t* col0 = stash + (half * 128 + cb) * HALF_M + row;  // [col][row]
 #pragma unroll
-              for (int i = 0; i < 64; ++i) {
-                uint32_t r = small_float_to_u8(__uint_as_float(i < 32 ? v[i] : w[i - 32]));
-                if (combine) {
-                  r += col0[i * HALF_M];
-                  r = (r >= mi) ? r - mi : r;
-                }
-                col0[i * HALF_M] = static_cast<uint8_t>(r);
-              }
+            for (int i = 0; i < 16; ++i) {
+              const float r0 = exact_mod(__uint_as_float(v[2 * i]), mf, inv);
+              const float r1 = exact_mod(__uint_as_float(v[2 * i + 1]), mf, inv);
+              // two residues as 16-bit lanes: low halves of 2^23 + r
+              const uint32_t p = __byte_perm(__float_as_uint(r0 + 8388608.0f), __float_as_uint(r1 + 8388608.0f),
+                                             0x5410);
+              const uint32_t s = __vadd2(run[cb * 16 + i], p);  // < 2m per lane
+              run[cb * 16 + i] = s - (__vcmpgeu2(s, mm2) & mm2);  // back into [0, m)
             }
           }
-          if (!final_chunk) tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
         }
         if (!ok) break;
-        // The finished half tile (128 rows x 256 columns) is in the stash: copy it out with
-        // coalesced 16-byte stores (column j of this half is 128 contiguous bytes of plane t).
+        // residues to the stash ([col][row] bytes), then coalesced 16-byte stores of the
+        // finished half tile (column j of this half is 128 contiguous bytes of plane t)
+        uint8_t* col0 = stash + (half * 128) * HALF_M + row;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          col0[(2 * i) * HALF_M] = static_cast<uint8_t>(run[i]);
+          col0[(2 * i + 1) * HALF_M] = static_cast<uint8_t>(run[i] >> 16);
+        }
         if (!epilogue_sync(epibar, eph)) {
           if (lane == 0) record_timeout(abort_flag);
           break;
