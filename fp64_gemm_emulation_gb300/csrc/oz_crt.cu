@@ -150,7 +150,24 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
     for (int t = 0; t < kMaxModuli; ++t)
       res[t] = (t < c.s) ? __ldg(reinterpret_cast<const uint32_t*>(base + t * plane)) : 0u;
     double* out = C + i0 + j * ldc;
-#pragma unroll 1
+    // Z = sum_t c_t P_t for the 4 elements at once (64-bit partial limbs, carries later):
+    // each constant limb P_t[l] is read once per 4 elements
+    uint64_t acc[4][NL];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int l = 0; l < NL; ++l) acc[e][l] = 0;
+#pragma unroll
+    for (int t = 0; t < kMaxModuli; ++t) {
+      if (t >= c.s) break;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t r = __byte_perm(res[t], 0u, 0x4440u | static_cast<uint32_t>(e));  // byte e
+#pragma unroll
+        for (int l = 0; l < NL; ++l) acc[e][l] += static_cast<uint64_t>(r) * c.P[t][l];
+      }
+    }
+#pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (i0 + e >= m) break;
       if (E[e] == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) {
@@ -161,23 +178,11 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         out[e] = 0.0;
         continue;
       }
-      // Z = sum_t c_t P_t with 64-bit partial limbs (carries resolved once, below)
-      uint64_t acc[NL];
-#pragma unroll
-      for (int l = 0; l < NL; ++l) acc[l] = 0;
-      const uint32_t sel = 0x4440u | static_cast<uint32_t>(e);
-#pragma unroll
-      for (int t = 0; t < kMaxModuli; ++t) {
-        if (t >= c.s) break;
-        const uint32_t r = __byte_perm(res[t], 0u, sel);  // byte e of res[t]
-#pragma unroll
-        for (int l = 0; l < NL; ++l) acc[l] += static_cast<uint64_t>(r) * c.P[t][l];
-      }
       uint32_t x[kLimbs];
       uint64_t carry = 0;
 #pragma unroll
       for (int l = 0; l < NL; ++l) {
-        const uint64_t v = acc[l] + carry;
+        const uint64_t v = acc[e][l] + carry;
         x[l] = static_cast<uint32_t>(v);
         carry = v >> 32;
       }

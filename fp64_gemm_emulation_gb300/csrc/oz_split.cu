@@ -77,18 +77,20 @@ __device__ __forceinline__ uint32_t residue_bf16(uint32_t x0, uint32_t x1, uint3
   return __float_as_uint(f) >> 16;
 }
 
-// Fast path (p == 0): bf16 bits of the symmetric residue of a' = +-u modulo m.
-//   ys = y, or BIG - y for a negative a' (BIG = m 2^22 > y, a multiple of m)
-//   v  = ys - m floor((ys + floor(m/2)) / m)   -- directly in [-floor(m/2), ceil(m/2) - 1]
-// where y = x2 c32 + x1 c16 + x0 == u (mod m), y < 2^30; ys + floor(m/2) < 2^30.
-__device__ __forceinline__ float residue_fast(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t negmask, uint32_t m,
-                                              uint32_t c16, uint32_t c32, uint32_t magic, uint32_t big,
-                                              uint32_t halfm) {
-  const uint32_t y = x2 * c32 + x1 * c16 + x0;
-  const uint32_t ys = (y ^ negmask) + (big & negmask) + (negmask & 1u);  // y or big - y
-  const uint32_t q = __umulhi(ys + halfm, magic) >> 7;
-  const int v = static_cast<int>(ys - q * m);
-  return __int_as_float(0x4B000080 + v) - 8388736.0f;  // exactly v
+// Fast path (p == 0): the symmetric residue of a' = sign * u modulo m, as a float.
+//   ys = sign * (x2 c32 + x1 c16 + x0) + neg * BIG + floor(m/2)   (BIG = m 2^22 > |y|)
+//   q  = floor(ys / m)                                            (one Barrett step)
+//   ys - q m = v + floor(m/2) with v the symmetric representative in
+//   [-floor(m/2), ceil(m/2) - 1]; the float 2^23 + 128 + v is built directly from the
+//   bits (the per-modulus constant absorbs floor(m/2)) and 2^23 + 128 subtracted.
+// sx* are the sign-applied 16-bit limbs of u, negf is 1 for a negative a'.
+__device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_t negf, uint32_t m, uint32_t c16,
+                                              uint32_t c32, uint32_t magic, uint32_t big, uint32_t halfm,
+                                              uint32_t fbase) {
+  const uint32_t y = static_cast<uint32_t>(sx2 * static_cast<int>(c32) + sx1 * static_cast<int>(c16) + sx0);
+  const uint32_t ys = negf * big + y + halfm;
+  const uint32_t q = __umulhi(ys, magic) >> 7;
+  return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
 
 template <bool kRowsContiguous>
@@ -146,19 +148,26 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
     for (int x = 0; x < 8; ++x) any_p |= (pp[x] != 0);
     if (!__any_sync(0xFFFFFFFFu, any_p)) {
       // common case: every a' of the warp is u itself (no power-of-two factor)
-      uint32_t nm[8];
+      int sx0[8], sx1[8], sx2[8];
+      uint32_t nf[8];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) nm[x] = ng[x] ? 0xFFFFFFFFu : 0u;
+      for (int x = 0; x < 8; ++x) {
+        const int sg = ng[x] ? -1 : 1;
+        sx0[x] = sg * static_cast<int>(x0[x]);
+        sx1[x] = sg * static_cast<int>(x1[x]);
+        sx2[x] = sg * static_cast<int>(x2[x]);
+        nf[x] = ng[x] ? 1u : 0u;
+      }
 #pragma unroll 1
       for (int t = 0; t < c.s; ++t) {
         const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-        const uint32_t big = m << 22, halfm = m >> 1;
+        const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
         uint32_t w[4];
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
-          const float lo = residue_fast(x0[2 * x], x1[2 * x], x2[2 * x], nm[2 * x], m, c16, c32, mg, big, halfm);
-          const float hi =
-              residue_fast(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], nm[2 * x + 1], m, c16, c32, mg, big, halfm);
+          const float lo = residue_fast(sx0[2 * x], sx1[2 * x], sx2[2 * x], nf[2 * x], m, c16, c32, mg, big, halfm, fbase);
+          const float hi = residue_fast(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], nf[2 * x + 1], m, c16, c32, mg,
+                                        big, halfm, fbase);
           w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
         }
         *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
