@@ -64,7 +64,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -163,7 +163,7 @@ def cpu_baseline_measure():
     from fp64_gemm_emulation_gb300.inputs import hpl_like
     from oracle import ozaki2 as O
 
-    ms, ns = 256, 256
+    ms, ns = 640, 640
     A, B = hpl_like(ms, ns, K, phi=PHI, seed=SEED)
     t0 = time.perf_counter()
     O.ozaki2_dgemm(A, B, S, keep=False)

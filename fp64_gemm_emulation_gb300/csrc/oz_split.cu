@@ -93,6 +93,70 @@ __device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
 
+// Residues of the 8 packed values of one thread modulo every modulus, written as 8 bf16
+// (16 bytes) per plane at dst + t * plane_elems.  Every lane of the warp must call it
+// (the p == 0 test is warp-uniform); lanes with dst == nullptr compute but do not store.
+__device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const SplitConsts& c, uint16_t* dst,
+                                                 long long plane_elems) {
+  // per element: 16-bit limbs of u, the shift p and the sign, shared by all moduli
+  uint32_t x0[8], x1[8], x2[8], pp[8];
+  bool ng[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const uint64_t u = v[x] & ((1ull << 53) - 1);
+    x0[x] = static_cast<uint32_t>(u) & 0xFFFFu;
+    x1[x] = static_cast<uint32_t>(u) >> 16;
+    x2[x] = static_cast<uint32_t>(u >> 32);
+    pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
+    ng[x] = (v[x] >> 63) != 0;
+  }
+  bool any_p = false;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) any_p |= (pp[x] != 0);
+  if (!__any_sync(0xFFFFFFFFu, any_p)) {
+    // common case: every a' of the warp is u itself (no power-of-two factor)
+    int sx0[8], sx1[8], sx2[8];
+    uint32_t nf[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int sg = ng[x] ? -1 : 1;
+      sx0[x] = sg * static_cast<int>(x0[x]);
+      sx1[x] = sg * static_cast<int>(x1[x]);
+      sx2[x] = sg * static_cast<int>(x2[x]);
+      nf[x] = ng[x] ? 1u : 0u;
+    }
+#pragma unroll 1
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
+      const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
+      uint32_t w[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float lo = residue_fast(sx0[2 * x], sx1[2 * x], sx2[2 * x], nf[2 * x], m, c16, c32, mg, big, halfm, fbase);
+        const float hi = residue_fast(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], nf[2 * x + 1], m, c16, c32, mg,
+                                      big, halfm, fbase);
+        w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
+      }
+      if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+#pragma unroll 1
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
+      uint32_t w[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t lo =
+            residue_bf16(x0[2 * x], x1[2 * x], x2[2 * x], pp[2 * x], ng[2 * x], m, c16, c32, mg);
+        const uint32_t hi = residue_bf16(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], pp[2 * x + 1],
+                                         ng[2 * x + 1], m, c16, c32, mg);
+        w[x] = lo | (hi << 16);
+      }
+      if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 template <bool kRowsContiguous>
 __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, const double* __restrict__ X,
                                                               long long rs, long long ks,
@@ -104,7 +168,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
   const int k0 = blockIdx.x * kSplitTile;
   const int r0 = blockIdx.y * kSplitTile;
 
-#pragma unroll 4
+#pragma unroll
   for (int it = 0; it < (kSplitTile * kSplitTile) / kSplitThreads; ++it) {
     int r, kk;
     if (kRowsContiguous) {
@@ -131,76 +195,53 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
 #pragma unroll
     for (int x = 0; x < 8; ++x) v[x] = tile[g * 8 + x][r];
     uint16_t* dst = planes + static_cast<long long>(r0 + r) * kp + k0 + g * 8;
-    // per element: 16-bit limbs of u, the shift p and the sign, shared by all moduli
-    uint32_t x0[8], x1[8], x2[8], pp[8];
-    bool ng[8];
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const uint64_t u = v[x] & ((1ull << 53) - 1);
-      x0[x] = static_cast<uint32_t>(u) & 0xFFFFu;
-      x1[x] = static_cast<uint32_t>(u) >> 16;
-      x2[x] = static_cast<uint32_t>(u >> 32);
-      pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
-      ng[x] = (v[x] >> 63) != 0;
-    }
-    bool any_p = false;
-#pragma unroll
-    for (int x = 0; x < 8; ++x) any_p |= (pp[x] != 0);
-    if (!__any_sync(0xFFFFFFFFu, any_p)) {
-      // common case: every a' of the warp is u itself (no power-of-two factor)
-      int sx0[8], sx1[8], sx2[8];
-      uint32_t nf[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        const int sg = ng[x] ? -1 : 1;
-        sx0[x] = sg * static_cast<int>(x0[x]);
-        sx1[x] = sg * static_cast<int>(x1[x]);
-        sx2[x] = sg * static_cast<int>(x2[x]);
-        nf[x] = ng[x] ? 1u : 0u;
-      }
-#pragma unroll 1
-      for (int t = 0; t < c.s; ++t) {
-        const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-        const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
-        uint32_t w[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float lo = residue_fast(sx0[2 * x], sx1[2 * x], sx2[2 * x], nf[2 * x], m, c16, c32, mg, big, halfm, fbase);
-          const float hi = residue_fast(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], nf[2 * x + 1], m, c16, c32, mg,
-                                        big, halfm, fbase);
-          w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
-        }
-        *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    } else {
-#pragma unroll 1
-      for (int t = 0; t < c.s; ++t) {
-        const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-        uint32_t w[4];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const uint32_t lo =
-              residue_bf16(x0[2 * x], x1[2 * x], x2[2 * x], pp[2 * x], ng[2 * x], m, c16, c32, mg);
-          const uint32_t hi = residue_bf16(x0[2 * x + 1], x1[2 * x + 1], x2[2 * x + 1], pp[2 * x + 1],
-                                           ng[2 * x + 1], m, c16, c32, mg);
-          w[x] = lo | (hi << 16);
-        }
-        *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
+    residues_to_planes(v, c, dst, plane_elems);
   }
+}
+
+// K-contiguous operand (B, column j = k contiguous): no transpose needed.  One thread
+// takes 8 consecutive k of one row: 64 contiguous bytes in, 16 contiguous bytes out per
+// modulus; a warp covers 256 consecutive k (2 KB read, 512 B written per plane).
+__global__ void __launch_bounds__(256) split_kcontig_kernel(int rows, int K, const double* __restrict__ X,
+                                                            long long ld, const int32_t* __restrict__ exps,
+                                                            const SplitConsts c, uint16_t* __restrict__ planes,
+                                                            int rows_padded, int kp) {
+  const int groups = kp >> 3;  // 8-k groups per row
+  const long long item = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = item < static_cast<long long>(rows_padded) * groups;  // all lanes stay for the vote
+  const int r = valid ? static_cast<int>(item / groups) : 0;
+  const int k0 = valid ? static_cast<int>(item - static_cast<long long>(r) * groups) * 8 : 0;
+  uint64_t v[8];
+  if (valid && r < rows) {
+    const int E = __ldg(exps + r);
+    const double* src = X + static_cast<long long>(r) * ld + k0;
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v[x] = (k0 + x < K) ? pack_scaled(__ldg(src + x), E, c.kA) : 0ull;
+  } else {
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v[x] = 0;
+  }
+  residues_to_planes(v, c, valid ? planes + static_cast<long long>(r) * kp + k0 : nullptr,
+                     static_cast<long long>(rows_padded) * kp);
 }
 
 cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,
                          const int32_t* exps, const SplitConsts& c, uint16_t* planes, int rows_padded, int kp,
                          cudaStream_t stream) {
-  dim3 grid(kp / kSplitTile, rows_padded / kSplitTile);
-  if (row_stride == 1)
+  if (row_stride == 1) {  // A: rows contiguous, transpose through shared memory
+    dim3 grid(kp / kSplitTile, rows_padded / kSplitTile);
     split_kernel<true><<<grid, kSplitThreads, 0, stream>>>(rows, k, X, row_stride, k_stride, exps, c, planes,
                                                            rows_padded, kp);
-  else
+  } else if (k_stride == 1) {  // B: K contiguous, direct
+    const long long items = static_cast<long long>(rows_padded) * (kp / 8);
+    split_kcontig_kernel<<<static_cast<unsigned>((items + 255) / 256), 256, 0, stream>>>(rows, k, X, row_stride,
+                                                                                        exps, c, planes,
+                                                                                        rows_padded, kp);
+  } else {
+    dim3 grid(kp / kSplitTile, rows_padded / kSplitTile);
     split_kernel<false><<<grid, kSplitThreads, 0, stream>>>(rows, k, X, row_stride, k_stride, exps, c, planes,
                                                             rows_padded, kp);
+  }
   return cudaGetLastError();
 }
 
