@@ -43,6 +43,10 @@ constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int STAGES = 6;
 constexpr int KB_PER_CHUNK = 16;  // 1024 k per chunk: |sum| <= 1024 * 2^14 = 2^24, exact in FP32
+// Scheduling K-block: whole K.  (Shorter K-blocks make the pairs' short panels fit L2 only
+// while the pairs run in lockstep; measured at 16384^3 they drift apart and DRAM reads rose
+// from 248 GB to 364 GB per launch, so each unit takes the whole k range.)
+constexpr int KB_PER_BLOCK = 1 << 24;
 constexpr uint32_t A_STAGE = HALF_M * BK * 2;
 constexpr uint32_t B_STAGE = HALF_N * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
@@ -111,6 +115,41 @@ __device__ __forceinline__ UnitCoord unit_coord(int u, int tiles_m, int tiles_n)
   return c;
 }
 
+// Work order of one CTA pair.  Its (tile, product) units are r = pair, pair + npairs, ...;
+// they are taken in groups of kGroup, and within a group K-block by K-block (every unit of
+// the group for K-block 0, then K-block 1, ...).  A K-block is kbb k-blocks of 64, so the
+// planes a wave of pairs touches at once are short panels that stay in L2, and the K-blocks
+// of one tile always follow each other on the same pair (their partial results are
+// combined in program order).
+constexpr int kGroup = 8;
+
+struct PairSchedule {
+  int pair, npairs, n_r, KB;
+  __device__ PairSchedule(int units, int nkb, int kbb) {
+    pair = static_cast<int>(blockIdx.x >> 1);
+    npairs = static_cast<int>(gridDim.x >> 1);
+    n_r = (units - pair + npairs - 1) / npairs;
+    KB = (nkb + kbb - 1) / kbb;
+  }
+  __device__ int count() const { return n_r * KB; }
+  __device__ void at(int idx, int& r, int& kb) const {
+    const int full = n_r / kGroup * kGroup;  // units in complete groups
+    int j;
+    if (idx < full * KB) {
+      const int g = idx / (kGroup * KB);
+      const int rem = idx - g * kGroup * KB;
+      kb = rem / kGroup;
+      j = g * kGroup + rem % kGroup;
+    } else {
+      const int gsz = n_r - full;
+      const int rem = idx - full * KB;
+      kb = rem / gsz;
+      j = full + rem % gsz;
+    }
+    r = pair + j * npairs;
+  }
+};
+
 constexpr int kModeResidue = 0;  // Scheme II: C''_t = (A'_t B'_t) mod m_t, uint8 output
 constexpr int kModeExact = 1;    // Scheme I: exact INT32 slice products
 
@@ -137,11 +176,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();      // 0 = leader of the pair, 1 = peer
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int tiles_m = mp / BM, tiles_n = np / BN;
   const int units = tiles_m * tiles_n * c.s;
   const int kbc = c.kb_per_chunk;
-  const int nchunks = (nkb + kbc - 1) / kbc;
+  const int kbb = c.kb_per_block;
+  const PairSchedule sched(units, nkb, kbb);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -175,13 +214,16 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (int u = pair; u < units && !*abort_flag; u += npairs) {
+      for (int idx = 0; idx < sched.count() && !*abort_flag; ++idx) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         const int pa = (MODE == kModeResidue) ? uc.t : c.a_plane[uc.t];
         const int pb = (MODE == kModeResidue) ? uc.t : c.b_plane[uc.t];
         const int rowA = uc.tm * BM + static_cast<int>(rank) * HALF_M;
         const int rowB = uc.tn * BN + static_cast<int>(rank) * HALF_N;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const int kb_end = min(nkb, (kblk + 1) * kbb);
+        for (int kb = kblk * kbb; kb < kb_end; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             record_timeout(abort_flag);
             break;
@@ -216,7 +258,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       uint32_t phase = 0;
       uint32_t g = 0;  // chunk counter: accumulator g & 1
       bool ok = true;
-      for (int u = pair; u < units && ok && !*abort_flag; u += npairs) {
+      for (int idx = 0; idx < sched.count() && ok && !*abort_flag; ++idx) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
+        const int kb_begin = kblk * kbb, kb_end = min(nkb, kb_begin + kbb);
+        const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
           const uint32_t acc = g & 1;
           if (!mbar_wait(&accempty[acc], ((g >> 1) & 1) ^ 1)) {
@@ -225,8 +271,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          const int kb0 = ch * kbc;
-          const int kb1 = min(nkb, kb0 + kbc);
+          const int kb0 = kb_begin + ch * kbc;
+          const int kb1 = min(kb_end, kb0 + kbc);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase)) {
               ok = false;
@@ -271,7 +317,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     bool ok = true;
     if (MODE == kModeExact) {
       int32_t* outp = static_cast<int32_t*>(out_ptr);
-      for (int u = pair; u < units && ok; u += npairs) {
+      for (int idx = 0; idx < sched.count() && ok; ++idx) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
+        const int kb_begin = kblk * kbb, kb_end = min(nkb, kb_begin + kbb);
+        const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         int32_t* base =
             outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row_off + row;
@@ -294,7 +344,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
               int32_t x = __float2int_rn(__uint_as_float(i < 32 ? v[i] : w[i - 32]));  // exact integer
-              if (ch > 0) x += o[static_cast<long long>(i) * mp];
+              if (kblk > 0 || ch > 0) x += o[static_cast<long long>(i) * mp];
               o[static_cast<long long>(i) * mp] = x;
             }
           }
@@ -305,7 +355,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       }
     } else {
       uint8_t* C_res = static_cast<uint8_t*>(out_ptr);
-      for (int u = pair; u < units && ok; u += npairs) {
+      for (int idx = 0; idx < sched.count() && ok; ++idx) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
+        const int kb_begin = kblk * kbb, kb_end = min(nkb, kb_begin + kbb);
+        const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         const float mf = c.modf[uc.t], inv = c.invf[uc.t];
         const uint32_t mm2 = static_cast<uint32_t>(mf) * 0x10001u;  // m in both 16-bit halves
@@ -345,19 +399,42 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
         }
         if (!ok) break;
-        // residues to the stash ([col][row] bytes), then coalesced 16-byte stores of the
-        // finished half tile (column j of this half is 128 contiguous bytes of plane t)
+        // This K-block's residues join the tile's running result in the stash ([col][row]
+        // bytes): for later K-blocks the previous result is first read back from the plane
+        // (16-byte loads, each thread the chunks it stored), then coalesced 16-byte stores.
+        uint8_t* dst = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM + row_off;
+        const uint32_t mi = static_cast<uint32_t>(mf);
+        if (kblk > 0) {
+#pragma unroll
+          for (int i = 0; i < (BN * HALF_M / 16) / EPI_THREADS; ++i) {
+            const int q = etid + i * EPI_THREADS;
+            const int col = q >> 3, part = q & 7;
+            *reinterpret_cast<uint4*>(stash + col * HALF_M + part * 16) =
+                *reinterpret_cast<const uint4*>(dst + static_cast<long long>(col) * mp + part * 16);
+          }
+          if (!epilogue_sync(epibar, eph)) {
+            if (lane == 0) record_timeout(abort_flag);
+            break;
+          }
+        }
         uint8_t* col0 = stash + (half * 128) * HALF_M + row;
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
-          col0[(2 * i) * HALF_M] = static_cast<uint8_t>(run[i]);
-          col0[(2 * i + 1) * HALF_M] = static_cast<uint8_t>(run[i] >> 16);
+          uint32_t lo = run[i] & 0xFFFFu, hi = run[i] >> 16;
+          if (kblk > 0) {
+            lo += col0[(2 * i) * HALF_M];
+            hi += col0[(2 * i + 1) * HALF_M];
+            lo = (lo >= mi) ? lo - mi : lo;
+            hi = (hi >= mi) ? hi - mi : hi;
+          }
+          col0[(2 * i) * HALF_M] = static_cast<uint8_t>(lo);
+          col0[(2 * i + 1) * HALF_M] = static_cast<uint8_t>(hi);
         }
         if (!epilogue_sync(epibar, eph)) {
           if (lane == 0) record_timeout(abort_flag);
           break;
         }
-        uint8_t* dst = C_res + uc.t * plane + static_cast<long long>(uc.tn) * BN * mp + uc.tm * BM + row_off;
+
 #pragma unroll
         for (int i = 0; i < (BN * HALF_M / 16) / EPI_THREADS; ++i) {
           const int q = etid + i * EPI_THREADS;
@@ -424,7 +501,9 @@ template <int MODE>
 static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
                        const uint16_t* A_planes, const uint16_t* B_planes, void* out, cudaStream_t stream) {
   using namespace gemm;
-  if (mp % BM || np % BN || kp % BK || c.kb_per_chunk < 1) return OZ_EINVAL;
+  if (mp % BM || np % BN || kp % BK || c.kb_per_chunk < 1 || c.kb_per_block < c.kb_per_chunk ||
+      c.kb_per_block % c.kb_per_chunk)
+    return OZ_EINVAL;
   CUtensorMap tmA, tmB;
   if (!make_plane_map(&tmA, A_planes, a_planes, mp, kp, HALF_M)) return OZ_ECUDA;
   if (!make_plane_map(&tmB, B_planes, b_planes, np, kp, HALF_N)) return OZ_ECUDA;
@@ -457,6 +536,7 @@ int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint1
                         const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream) {
   GemmConsts cc = c;
   cc.kb_per_chunk = gemm::KB_PER_CHUNK;
+  cc.kb_per_block = gemm::KB_PER_BLOCK;
   return launch_gemm<kModeResidue>(mp, np, kp, c.s, c.s, cc, A_planes, B_planes, C_res, stream);
 }
 

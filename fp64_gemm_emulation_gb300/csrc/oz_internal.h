@@ -47,6 +47,7 @@ constexpr int kMaxPairs = OZ_MAX_SLICES * (OZ_MAX_SLICES + 1) / 2;  // Scheme I 
 struct GemmConsts {
   int s;              // number of products
   int kb_per_chunk;   // k-blocks of 64 whose FP32 sum stays exact
+  int kb_per_block;   // k-blocks of 64 per scheduling K-block (a multiple of kb_per_chunk)
   float modf[kMaxModuli];
   float invf[kMaxModuli];
   uint8_t a_plane[kMaxPairs];

@@ -212,6 +212,7 @@ GemmConsts pair_consts(int s, int beta) {
   // products of slices are <= 2^(2 beta - 2): 2^(26 - 2 beta) of them stay below 2^24
   const long long chunk_k = 1ll << (26 - 2 * beta);
   g.kb_per_chunk = static_cast<int>(chunk_k / 64 > 0 ? chunk_k / 64 : 1);
+  g.kb_per_block = g.kb_per_chunk * ((1 << 24) / g.kb_per_chunk);  // whole k range per unit
   return g;
 }
 
