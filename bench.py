@@ -99,6 +99,34 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ DRAM traffic of the GEMM
+GEMM_SOURCES = ["fp64_gemm_emulation_gb300/csrc/oz_gemm.cu", "fp64_gemm_emulation_gb300/csrc/oz_device.cuh",
+                "fp64_gemm_emulation_gb300/csrc/oz_internal.h"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "residue_gemm_16384_s14_traffic.json")
+
+
+def gemm_source_digest() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in GEMM_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic_bytes():
+    """dram__bytes_read.sum + dram__bytes_write.sum of one residue-GEMM launch at this
+    workload, from the committed ncu capture; None if the kernel sources changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    if rec.get("source_sha256") != gemm_source_digest():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
 # ------------------------------------------------------------------ distributed helpers
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -255,11 +283,7 @@ def run_ours(args, world, rank, local):
     int_ops = S * 2.0 * M * N * K
     peak_t = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     achieved = int_ops / (gemm_ms * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("residue_gemm_16384_s14_bytes_per_launch")
+    traffic = gemm_traffic_bytes()
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
                 "frac": achieved / peak_t, "traffic": traffic,
                 "kernel": "oz::residue_gemm_kernel (s x 2mnk exact integer products on tcgen05 BF16)",
@@ -320,7 +344,8 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu_baseline_measure() if not args.no_cpu_baseline else None,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": clk, "context": context,
-            "tensor_path": "residues in bf16, exact FP32 accumulation in TMEM, folded mod m_t every 960 k",
+            "tensor_path": "residues in bf16 on tcgen05 CTA pairs, exact FP32 accumulation in TMEM over "
+                           "chunks of 1024 k, each chunk reduced mod m_t into register residues",
             "vs_baseline_ref": "pages' GH200 Scheme II figure, 80.2 TFLOPS (other hardware)",
         }
         print(json.dumps(line), flush=True)

@@ -238,6 +238,26 @@ void keep_default_pool_cached() {
   done[dev] = true;
 }
 
+// A dimension cut into up to kMax blocks whose sizes are multiples of 256 (but the last).
+struct Blocks {
+  static constexpr int kMax = 8;
+  int count;
+  int start[kMax], size[kMax];
+};
+
+Blocks make_blocks(int d, int want) {
+  Blocks b{};
+  if (want < 1) want = 1;
+  if (want > Blocks::kMax) want = Blocks::kMax;
+  const int bs = static_cast<int>(roundup((d + want - 1) / want, 256));
+  for (int s0 = 0; s0 < d && b.count < Blocks::kMax; s0 += bs) {
+    b.start[b.count] = s0;
+    b.size[b.count] = (d - s0 < bs) ? d - s0 : bs;
+    ++b.count;
+  }
+  return b;
+}
+
 GemmConsts make_gemm_consts(const SplitConsts& sc) {
   GemmConsts g{};
   g.s = sc.s;
@@ -390,32 +410,143 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
   if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
   if (m == 0 || n == 0) return OZ_OK;
   if (!C || (k > 0 && (!A || !B))) return OZ_EINVAL;
-  cudaStream_t st;
-  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return OZ_ECUDA;
+  if (k == 0) {  // C = +0 (BLAS with beta = 0); host memory
+    for (int j = 0; j < n; ++j) std::memset(C + static_cast<size_t>(j) * ldc, 0, sizeof(double) * m);
+    return OZ_OK;
+  }
+  {
+    int kA;
+    if ((rc = ozaki2_choose_k(num_moduli, k, &kA))) return rc;
+  }
+  // Two-dimensional block pipeline: row blocks of A x column blocks of B.  Copies in on one
+  // stream, the path on a second, copies out on a third, so block (i, j) computes while the
+  // next operand blocks arrive and finished blocks of C leave.
+  const int s = num_moduli;
+  const Blocks mb = make_blocks(m, m >= 4096 ? 2 : 1);
+  const Blocks nbk = make_blocks(n, n >= 8192 ? 4 : (n >= 2048 ? 2 : 1));
+  const int kp = static_cast<int>(roundup(k, kPadK));
+  size_t off = 0;
+  const size_t off_dA = off;
+  off = align256(off + sizeof(double) * static_cast<size_t>(m) * k);
+  const size_t off_dB = off;
+  off = align256(off + sizeof(double) * static_cast<size_t>(k) * n);
+  const size_t off_dC = off;
+  off = align256(off + sizeof(double) * static_cast<size_t>(m) * n);
+  const size_t off_rowexp = off;
+  off = align256(off + sizeof(int32_t) * m);
+  const size_t off_colexp = off;
+  off = align256(off + sizeof(int32_t) * n);
+  size_t off_Ap[Blocks::kMax], off_Bp[Blocks::kMax];
+  int max_mp = 0, max_np = 0;
+  for (int i = 0; i < mb.count; ++i) {
+    const int mpi = static_cast<int>(roundup(mb.size[i], kPadM));
+    max_mp = mpi > max_mp ? mpi : max_mp;
+    off_Ap[i] = off;
+    off = align256(off + sizeof(uint16_t) * static_cast<size_t>(s) * mpi * kp);
+  }
+  for (int j = 0; j < nbk.count; ++j) {
+    const int npj = static_cast<int>(roundup(nbk.size[j], kPadN));
+    max_np = npj > max_np ? npj : max_np;
+    off_Bp[j] = off;
+    off = align256(off + sizeof(uint16_t) * static_cast<size_t>(s) * npj * kp);
+  }
+  const size_t off_Cr = off;
+  off = align256(off + static_cast<size_t>(s) * max_mp * max_np);
+  const size_t total = off;
+
+  cudaStream_t sin = nullptr, scomp = nullptr, sout = nullptr;
+  if (cudaStreamCreateWithFlags(&sin, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&scomp, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&sout, cudaStreamNonBlocking) != cudaSuccess) {
+    if (sin) cudaStreamDestroy(sin);
+    if (scomp) cudaStreamDestroy(scomp);
+    cudaGetLastError();
+    return OZ_ECUDA;
+  }
   keep_default_pool_cached();
-  const size_t a_bytes = sizeof(double) * static_cast<size_t>(lda) * (k > 0 ? k : 1);
-  const size_t b_bytes = sizeof(double) * static_cast<size_t>(ldb) * n;
-  const size_t c_bytes = sizeof(double) * static_cast<size_t>(ldc) * n;
-  double *dA = nullptr, *dB = nullptr, *dC = nullptr;
-  rc = OZ_OK;
-  if (cudaMallocAsync(&dA, a_bytes, st) != cudaSuccess || cudaMallocAsync(&dB, b_bytes, st) != cudaSuccess ||
-      cudaMallocAsync(&dC, c_bytes, st) != cudaSuccess)
-    rc = OZ_ENOMEM;
-  if (!rc && k > 0) {
-    if (cudaMemcpyAsync(dA, A, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  cudaEvent_t ev[2 * Blocks::kMax + Blocks::kMax * Blocks::kMax] = {};
+  const int nev = mb.count + nbk.count + mb.count * nbk.count;
+  for (int e = 0; e < nev && !rc; ++e)
+    if (cudaEventCreateWithFlags(&ev[e], cudaEventDisableTiming) != cudaSuccess) rc = OZ_ECUDA;
+  cudaEvent_t* evA = ev;
+  cudaEvent_t* evB = ev + mb.count;
+  cudaEvent_t* evC = ev + mb.count + nbk.count;
+
+  uint8_t* ws = nullptr;
+  if (!rc && cudaMallocAsync(reinterpret_cast<void**>(&ws), total, scomp) != cudaSuccess) rc = OZ_ENOMEM;
+  cudaEvent_t ready = nullptr;  // the allocation is ordered on scomp: the copy streams wait for it
+  if (!rc && (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess ||
+              cudaEventRecord(ready, scomp) != cudaSuccess || cudaStreamWaitEvent(sin, ready, 0) != cudaSuccess))
+    rc = OZ_ECUDA;
+  double* dA = reinterpret_cast<double*>(ws + off_dA);
+  double* dB = reinterpret_cast<double*>(ws + off_dB);
+  double* dC = reinterpret_cast<double*>(ws + off_dC);
+  int32_t* rowexp = reinterpret_cast<int32_t*>(ws + off_rowexp);
+  int32_t* colexp = reinterpret_cast<int32_t*>(ws + off_colexp);
+  uint8_t* Cr = ws + off_Cr;
+
+  // copies in: A_0, B_0 .. B_last, A_1 .. A_last (the order the blocks are consumed)
+  auto copy_A = [&](int i) {
+    if (!rc && (cudaMemcpy2DAsync(dA + mb.start[i], sizeof(double) * m, A + mb.start[i], sizeof(double) * lda,
+                                  sizeof(double) * mb.size[i], k, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+                cudaEventRecord(evA[i], sin) != cudaSuccess))
+      rc = OZ_ECUDA;
+  };
+  copy_A(0);
+  for (int j = 0; j < nbk.count && !rc; ++j) {
+    if (cudaMemcpy2DAsync(dB + static_cast<size_t>(nbk.start[j]) * k, sizeof(double) * k,
+                          B + static_cast<size_t>(nbk.start[j]) * ldb, sizeof(double) * ldb, sizeof(double) * k,
+                          nbk.size[j], cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+        cudaEventRecord(evB[j], sin) != cudaSuccess)
       rc = OZ_ECUDA;
   }
-  if (!rc && ldc != m) {  // keep the caller's padding rows of C intact
-    if (cudaMemcpyAsync(dC, C, c_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) rc = OZ_ECUDA;
+  for (int i = 1; i < mb.count; ++i) copy_A(i);
+
+  // the path, block by block
+  for (int i = 0; i < mb.count && !rc; ++i) {
+    const int i0 = mb.start[i], mi = mb.size[i];
+    uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + off_Ap[i]);
+    if (cudaStreamWaitEvent(scomp, evA[i], 0) != cudaSuccess) rc = OZ_ECUDA;
+    if (!rc) rc = ozaki2_exponents(mi, 0, k, dA + i0, m, nullptr, 1, rowexp + i0, nullptr, scomp);
+    if (!rc) rc = ozaki2_split(mi, 0, k, dA + i0, m, nullptr, 1, s, rowexp + i0, nullptr, Ap, nullptr, scomp);
+    for (int j = 0; j < nbk.count && !rc; ++j) {
+      const int j0 = nbk.start[j], nj = nbk.size[j];
+      uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + off_Bp[j]);
+      const double* dBj = dB + static_cast<size_t>(j0) * k;
+      if (i == 0) {
+        if (cudaStreamWaitEvent(scomp, evB[j], 0) != cudaSuccess) rc = OZ_ECUDA;
+        if (!rc) rc = ozaki2_exponents(0, nj, k, nullptr, 1, dBj, k, nullptr, colexp + j0, scomp);
+        if (!rc) rc = ozaki2_split(0, nj, k, nullptr, 1, dBj, k, s, nullptr, colexp + j0, nullptr, Bp, scomp);
+      }
+      if (!rc) rc = ozaki2_residue_gemm(mi, nj, k, s, Ap, Bp, Cr, scomp);
+      double* dCij = dC + i0 + static_cast<size_t>(j0) * m;
+      if (!rc) rc = ozaki2_crt(mi, nj, k, s, Cr, rowexp + i0, colexp + j0, dCij, m, scomp);
+      cudaEvent_t e = evC[i * nbk.count + j];
+      if (!rc && (cudaEventRecord(e, scomp) != cudaSuccess || cudaStreamWaitEvent(sout, e, 0) != cudaSuccess ||
+                  cudaMemcpy2DAsync(C + i0 + static_cast<size_t>(j0) * ldc, sizeof(double) * ldc, dCij,
+                                    sizeof(double) * m, sizeof(double) * mi, nj, cudaMemcpyDeviceToHost,
+                                    sout) != cudaSuccess))
+        rc = OZ_ECUDA;
+      (void)kp;
+    }
   }
-  if (!rc) rc = ozaki2_dgemm(m, n, k, dA, lda, dB, ldb, dC, ldc, num_moduli, st);
-  if (!rc && cudaMemcpyAsync(C, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) rc = OZ_ECUDA;
-  if (dA) cudaFreeAsync(dA, st);
-  if (dB) cudaFreeAsync(dB, st);
-  if (dC) cudaFreeAsync(dC, st);
-  if (cudaStreamSynchronize(st) != cudaSuccess && !rc) rc = OZ_ECUDA;
-  cudaStreamDestroy(st);
+  // release the workspace after the copies out, then wait for everything
+  cudaEvent_t done = nullptr;
+  if (ws) {
+    if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess && cudaEventRecord(done, sout) == cudaSuccess)
+      cudaStreamWaitEvent(scomp, done, 0);
+    cudaFreeAsync(ws, scomp);
+  }
+  if (cudaStreamSynchronize(sin) != cudaSuccess && !rc) rc = OZ_ECUDA;
+  if (cudaStreamSynchronize(sout) != cudaSuccess && !rc) rc = OZ_ECUDA;
+  if (cudaStreamSynchronize(scomp) != cudaSuccess && !rc) rc = OZ_ECUDA;
+  for (int e = 0; e < nev; ++e)
+    if (ev[e]) cudaEventDestroy(ev[e]);
+  if (ready) cudaEventDestroy(ready);
+  if (done) cudaEventDestroy(done);
+  cudaStreamDestroy(sin);
+  cudaStreamDestroy(scomp);
+  cudaStreamDestroy(sout);
   cudaGetLastError();
   return rc;
 }

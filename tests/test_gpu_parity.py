@@ -212,3 +212,25 @@ def test_deterministic_repeats(oz):
     dA, dB = dev(A), dev(B)
     outs = [bits(host(oz.ozaki2_dgemm(dA, dB, 14))) for _ in range(3)]
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
+
+
+def test_host_pipeline_blocks_match_device_path(oz):
+    # m >= 4096 and n >= 2048: the host entry point splits A into 2 row blocks and B into
+    # 2 column blocks (ragged last blocks) and overlaps copies with compute; the result
+    # must equal the device-resident entry point bit for bit, with padded leading dims.
+    m, n, k = 4300, 2600, 700
+    A, B = hpl_like(m, n, k, phi=1.0, seed=17)
+    Ah = np.zeros((m + 5, k), order="F")
+    Ah[:m] = A
+    Bh = np.zeros((k + 3, n), order="F")
+    Bh[:k] = B
+    Ch = np.full((m + 7, n), -2.0, order="F")
+    rc = oz._lib.ozaki2_dgemm_host(m, n, k, Ah.ctypes.data, m + 5, Bh.ctypes.data, k + 3, Ch.ctypes.data, m + 7, 14)
+    assert rc == 0
+    ref = host(oz.ozaki2_dgemm(dev(A), dev(B), 14))
+    assert np.array_equal(bits(Ch[:m]), bits(ref))
+    assert np.all(Ch[m:] == -2.0)
+    # sampled entries against the oracle as well
+    rows, cols = [0, m - 1, 4095, 4096, 17], [n - 1, 0, 2047, 2048, 1000]
+    want = O.direct_entries(A, B, 14, rows, cols)
+    assert np.array_equal(bits(Ch[rows, cols]), bits(want))
