@@ -63,6 +63,21 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ int g_status = 0;
 
+// Pair pacing (never needed for correctness).  Every kPaceEvery k-blocks a pair leader's
+// producer adds 1 to its launch's counter and compares its own count with the pairs'
+// average (the counter value it loaded at the previous checkpoint, so the load latency is
+// hidden); a producer more than kPaceWindow checkpoints ahead pauses, for at most
+// kPaceLimitNs.  Pairs that share plane panels then stream them at about the same time,
+// so the panels are read from DRAM once and served to the others from L2.  A finished
+// pair adds a large credit so the tail of the launch never waits.  The counter slot of
+// a launch is zeroed on its stream just before it starts.
+constexpr int kPaceSlots = 64;
+constexpr uint32_t kPaceEvery = 16;
+constexpr uint32_t kPaceWindow = 2;
+constexpr uint32_t kPaceDoneCredit = 1u << 24;
+constexpr uint64_t kPaceLimitNs = 100000;
+__device__ unsigned int g_pace_ctr[kPaceSlots];
+
 int* device_status_ptr() {
   int* p = nullptr;
   cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status);
@@ -214,6 +229,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
+      const bool pacer = (rank == 0);
+      unsigned int* ctr = &g_pace_ctr[c.launch_id % kPaceSlots];
+      uint32_t paced = 0, checkpoints = 0, seen = 0;
       for (int idx = 0; idx < sched.count() && !*abort_flag; ++idx) {
         int u, kblk;
         sched.at(idx, u, kblk);
@@ -237,8 +255,22 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             stage = 0;
             phase ^= 1;
           }
+          if (pacer && ++paced % kPaceEvery == 0) {
+            ++checkpoints;
+            atomicAdd(ctr, 1u);
+            const uint32_t np = static_cast<uint32_t>(sched.npairs);
+            if (checkpoints * np > seen + kPaceWindow * np) {  // ahead of the average: pause
+              const uint64_t t0 = globaltimer_ns();
+              while (checkpoints * np > seen + kPaceWindow * np && globaltimer_ns() - t0 < kPaceLimitNs) {
+                __nanosleep(256);
+                seen = *reinterpret_cast<volatile unsigned int*>(ctr);
+              }
+            }
+            seen = *reinterpret_cast<volatile unsigned int*>(ctr);  // used at the next checkpoint
+          }
         }
       }
+      if (pacer) atomicAdd(ctr, kPaceDoneCredit);  // finished: nobody waits for this pair
       // Every issued copy must have landed before the pair may exit; the MMA thread has
       // consumed them on the normal path.  The copies complete on the leader's barriers,
       // which the leader's MMA thread drains (below); here wait for this CTA's stages to
@@ -497,6 +529,11 @@ static bool make_plane_map(CUtensorMap* map, const void* base, int s, int rows, 
   return r == CUDA_SUCCESS;
 }
 
+static uint32_t next_launch_id() {
+  static uint32_t id = 0;
+  return __atomic_add_fetch(&id, 1u, __ATOMIC_RELAXED);
+}
+
 template <int MODE>
 static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
                        const uint16_t* A_planes, const uint16_t* B_planes, void* out, cudaStream_t stream) {
@@ -528,7 +565,16 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int nkb = kp / BK;
-  if (cudaLaunchKernelEx(&cfg, residue_gemm_kernel<MODE>, tmA, tmB, c, out, mp, np, nkb) != cudaSuccess) return OZ_ECUDA;
+  GemmConsts cl = c;
+  cl.launch_id = next_launch_id();
+  {  // zero this launch's pacing counter on the stream
+    unsigned int* ctr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ctr), g_pace_ctr) != cudaSuccess) return OZ_ECUDA;
+    if (cudaMemsetAsync(ctr + cl.launch_id % kPaceSlots, 0, sizeof(unsigned int), stream) != cudaSuccess)
+      return OZ_ECUDA;
+  }
+  if (cudaLaunchKernelEx(&cfg, residue_gemm_kernel<MODE>, tmA, tmB, cl, out, mp, np, nkb) != cudaSuccess)
+    return OZ_ECUDA;
   return cudaGetLastError() == cudaSuccess ? OZ_OK : OZ_ECUDA;
 }
 

@@ -48,6 +48,7 @@ struct GemmConsts {
   int s;              // number of products
   int kb_per_chunk;   // k-blocks of 64 whose FP32 sum stays exact
   int kb_per_block;   // k-blocks of 64 per scheduling K-block (a multiple of kb_per_chunk)
+  uint32_t launch_id; // selects this launch's pacing counter
   float modf[kMaxModuli];
   float invf[kMaxModuli];
   uint8_t a_plane[kMaxPairs];
