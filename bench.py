@@ -154,6 +154,28 @@ def barrier(world: int):
         dist.barrier()
 
 
+# ------------------------------------------------------------------ host link
+def host_link_gbs(h_in, h_out, device) -> dict:
+    """Pinned host<->device copy bandwidth of this machine (context for the e2e figure)."""
+    import torch
+
+    a, b = h_in.reshape(-1), h_out.reshape(-1)
+    d = torch.empty(max(a.numel(), b.numel()), dtype=a.dtype, device=device)
+    out = {}
+    for name, copy, nbytes in (("h2d", lambda: d[: a.numel()].copy_(a, non_blocking=True), a.numel() * a.element_size()),
+                               ("d2h", lambda: b.copy_(d[: b.numel()], non_blocking=True), b.numel() * b.element_size())):
+        copy()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        copy()
+        e1.record()
+        torch.cuda.synchronize(device)
+        out[name] = nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del d
+    return out
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 def run_reference(args, world, rank):
     if rank != 0:
@@ -313,7 +335,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
     e2e = {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": 8 * (M * K + K * N), "d2h_bytes_per_step": 8 * M * N,
-           "api": "ozaki2_dgemm_host (pinned host A, B, C; copies inside the timed region)"}
+           "api": "ozaki2_dgemm_host (pinned host A, B, C; copies inside the timed region)",
+           "host_link_gbs": host_link_gbs(hA, hC, device)}
 
     # ---- context: native FP64 GEMM (cuBLAS through torch) on the same GPU, one call
     context = {}

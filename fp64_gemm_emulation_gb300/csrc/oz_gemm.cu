@@ -72,8 +72,8 @@ __device__ int g_status = 0;
 // pair adds a large credit so the tail of the launch never waits.  The counter slot of
 // a launch is zeroed on its stream just before it starts.
 constexpr int kPaceSlots = 64;
-constexpr uint32_t kPaceEvery = 16;
-constexpr uint32_t kPaceWindow = 2;
+constexpr uint32_t kPaceEvery = 8;
+constexpr uint32_t kPaceWindow = 1;
 constexpr uint32_t kPaceDoneCredit = 1u << 24;
 constexpr uint64_t kPaceLimitNs = 100000;
 __device__ unsigned int g_pace_ctr[kPaceSlots];
