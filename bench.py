@@ -54,10 +54,10 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, tag: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks{tag}_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -325,17 +325,27 @@ def run_ours(args, world, rank, local):
     hA = torch.from_numpy(A_np.T.copy()).pin_memory()   # column-major A as a (k, m) row-major block
     hB = torch.from_numpy(B_np.T.copy()).pin_memory()
     hC = torch.empty((N, M), dtype=torch.float64).pin_memory()
-    e2e_steps = max(1, min(args.steps, 3))
+    e2e_steps = args.steps
     oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)  # warm-up
+    e2e_clocks = ClockSampler(local, "_e2e")
+    e2e_clocks.start()
+    time.sleep(0.3)
     barrier(world)
+    call_ms = []
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
+        t1 = time.perf_counter()
         oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)
+        call_ms.append(1e3 * (time.perf_counter() - t1))
     e2e_s = reduce_max(time.perf_counter() - t0, world, device)
     barrier(world)
+    e2e_clk = e2e_clocks.stop()
     e2e = {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": 8 * (M * K + K * N), "d2h_bytes_per_step": 8 * M * N,
            "api": "ozaki2_dgemm_host (pinned host A, B, C; copies inside the timed region)",
+           "steps": e2e_steps,
+           "call_ms": {"min": min(call_ms), "median": statistics.median(call_ms), "max": max(call_ms)},
+           "clocks": e2e_clk,
            "host_link_gbs": host_link_gbs(hA, hC, device)}
 
     # ---- context: native FP64 GEMM (cuBLAS through torch) on the same GPU, one call
