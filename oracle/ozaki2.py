@@ -272,6 +272,176 @@ def unscale(C3: np.ndarray, d: list[int], e: list[int], rowflag=None, colflag=No
 
 
 # --------------------------------------------------------------------------
+# Range estimation variants ([Ozaki II, §9]): OS II-fast and OS II-accu
+# --------------------------------------------------------------------------
+# The CRT result is unique when c_max >= max_ij (|A'||B'|)_ij stays <= M/2 - 1
+# ([Ozaki II, §5, §9]).  The uniform estimate above takes c_max = q 2^(k_A+k_B).
+# OS II-fast bounds (|A'||B'|)_ij by the Cauchy-Schwarz product of a row norm of A'
+# and a column norm of B'; OS II-accu bounds it entry by entry with an exact
+# low-precision product of rounded-up magnitudes.  Both keep the form
+# d_i = kappa - t_i with kappa the largest k such that 2^(2k) <= M/2 - 1 (the k of
+# q = 1) and a per-row exponent t_i; everything after the exponents is unchanged.
+SCALINGS = ("uniform", "fast", "accu")
+NORM_GUARD = 16  # G: entries below 2^-G of the row maximum count as 4^-G of its square
+
+
+def half_range_log2(M: int) -> int:
+    """L = floor(log2(M/2 - 1)): the largest L with 2^L <= M/2 - 1 (i.e. 2^(L+1) <= M - 2)."""
+    if M - 2 < 2:
+        raise ValueError("M too small")
+    return (M - 2).bit_length() - 2
+
+
+def ceil_log2_int(x: int) -> int:
+    """ceil(log2 x) for an integer x >= 1."""
+    if x < 1:
+        raise ValueError("need x >= 1")
+    return (int(x) - 1).bit_length()
+
+
+def norm_exponents(X: np.ndarray) -> list:
+    """OS II-fast: per row, an integer t with 2^t >= ||x_i||_2 (None / 'nan' as in row_exponents).
+
+    Each |x_ik| <= 2^c_k with c_k = ceil(log2 |x_ik|) exact from the bits, so
+    ||x_i||^2 <= sum_k 4^c_k <= 4^(c_max - G) S,  S = sum_k max(1, 4^(c_k - c_max + G)),
+    an integer (order-free), and ||x_i|| <= 2^(c_max - G + ceil(ceil(log2 S) / 2)) = 2^t.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    finite = np.isfinite(X).all(axis=1)
+    out: list = []
+    for i in range(X.shape[0]):
+        if not finite[i]:
+            out.append("nan")
+            continue
+        row = X[i][X[i] != 0]
+        if row.size == 0:
+            out.append(ZERO_ROW)
+            continue
+        c = _ceil_log2_abs_array(row)
+        cmax = int(c.max())
+        delta = c - cmax + NORM_GUARD  # <= G
+        S = sum(4 ** int(dv) if dv >= 0 else 1 for dv in delta)
+        L = ceil_log2_int(S)
+        out.append(cmax - NORM_GUARD + (L + 1) // 2)
+    return out
+
+
+def accu_bits(q: int) -> int:
+    """OS II-accu: b = the largest integer in [0, 7] with q 4^b <= 2^24.
+
+    Bound entries are integers in [0, 2^b]; their products (<= 4^b) summed over q
+    stay <= 2^24, so one FP32 accumulation (or any integer arithmetic) is exact.
+    """
+    if q < 1 or q > 2**24:
+        raise ValueError("OS II-accu needs 1 <= q <= 2^24")
+    b = 0
+    while b < 7 and q * 4 ** (b + 1) <= 2**24:
+        b += 1
+    return b
+
+
+def magnitude_bounds(X: np.ndarray, E: list, b: int) -> np.ndarray:
+    """X^_ik = ceil(|x_ik| 2^(b - E_i)) in [0, 2^b] (int64); rows without an exponent are 0.
+
+    With E_i = ceil(log2 max_k |x_ik|) this is |x_ik| rounded up to b bits of the
+    row's range: |x_ik| <= X^_ik 2^(E_i - b).
+    """
+    X = np.asarray(X, dtype=np.float64)
+    out = np.zeros(X.shape, dtype=np.int64)
+    f, e = np.frexp(np.abs(np.where(np.isfinite(X), X, 0.0)))
+    sig = np.ldexp(f, 53).astype(np.int64)  # |x| = sig 2^(e - 53), exact
+    for i in range(X.shape[0]):
+        if E[i] is ZERO_ROW or E[i] == "nan":
+            continue
+        sh = e[i].astype(np.int64) - 53 + b - int(E[i])  # |x| 2^(b - E) = sig 2^sh
+        right = -sh
+        small = right >= 62
+        r = np.clip(right, 0, 61)
+        up = np.where(right > 0, (sig[i] + (np.int64(1) << r) - 1) >> r, sig[i] << np.clip(sh, 0, 61))
+        up = np.where(small, (sig[i] > 0).astype(np.int64), up)
+        out[i] = np.where(sig[i] > 0, up, 0)
+    return out
+
+
+def accu_exponents(A: np.ndarray, B: np.ndarray, M: int):
+    """OS II-accu exponents: (kappa, tA, tB, b, Ahat, Bhat, Chat).
+
+    C^ = A^ B^ (exact integers) bounds sum_k |a_ik||b_kj| <= 2^(E_i + F_j - 2b) C^_ij.
+    With rho_i = max(1, max_j C^_ij), gamma_j = max(1, max_i C^_ij), L as in
+    half_range_log2 and x_i = floor((L - ceil(log2 rho_i)) / 2), y_j likewise,
+    d_i = x_i - E_i + b and e_j = y_j - F_j + b give
+    (|A'||B'|)_ij <= 2^(x_i + y_j) C^_ij <= 2^L <= M/2 - 1, because
+    C^_ij <= min(rho_i, gamma_j) <= 2^((ceil log2 rho_i + ceil log2 gamma_j) / 2).
+    Returned as t_i = kappa - d_i (kappa = floor(L/2)).
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    q = A.shape[1]
+    b = accu_bits(q)
+    EA = row_exponents(A)
+    EB = row_exponents(B.T)
+    Ahat = magnitude_bounds(A, EA, b)
+    Bhat = magnitude_bounds(B.T, EB, b)  # n x q
+    Chat = exact_int_matmul(Ahat, Bhat.T)
+    L = half_range_log2(M)
+    kap = L // 2
+    rho = np.maximum(Chat.max(axis=1, initial=0), 1)
+    gamma = np.maximum(Chat.max(axis=0, initial=0), 1)
+    tA = [E if (E is ZERO_ROW or E == "nan") else kap - (L - ceil_log2_int(int(r))) // 2 + E - b
+          for E, r in zip(EA, rho)]
+    tB = [F if (F is ZERO_ROW or F == "nan") else kap - (L - ceil_log2_int(int(g))) // 2 + F - b
+          for F, g in zip(EB, gamma)]
+    return kap, tA, tB, b, Ahat, Bhat, Chat
+
+
+def accu_exponents_sampled(A: np.ndarray, B: np.ndarray, M: int, rows, cols):
+    """accu_exponents for selected rows of A and columns of B only (same values).
+
+    rho_i needs row i of C^ in full and gamma_j column j, i.e. A^[i] B^ and A^ B^[:, j]:
+    vector-matrix products, cheap enough for sampled checks of large problems.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    q = A.shape[1]
+    b = accu_bits(q)
+    EA = row_exponents(A)
+    EB = row_exponents(B.T)
+    Ahat = magnitude_bounds(A, EA, b).astype(np.float64)  # integers <= 2^7: exact
+    BhatT = magnitude_bounds(B.T, EB, b).astype(np.float64)
+    L = half_range_log2(M)
+    kap = L // 2
+    tA, tB = {}, {}
+    for i in set(int(r) for r in rows):
+        E = EA[i]
+        if E is ZERO_ROW or E == "nan":
+            tA[i] = E
+            continue
+        rho = max(int((BhatT @ Ahat[i]).max(initial=0)), 1)  # sums <= 2^24: exact in float64
+        tA[i] = kap - (L - ceil_log2_int(rho)) // 2 + E - b
+    for j in set(int(c) for c in cols):
+        F = EB[j]
+        if F is ZERO_ROW or F == "nan":
+            tB[j] = F
+            continue
+        gamma = max(int((Ahat @ BhatT[j]).max(initial=0)), 1)
+        tB[j] = kap - (L - ceil_log2_int(gamma)) // 2 + F - b
+    return kap, tA, tB
+
+
+def scaling_exponents(A: np.ndarray, B: np.ndarray, M: int, scaling: str):
+    """(k, EA, EB) of a scaling mode: d_i = k - EA_i, e_j = k - EB_j."""
+    q = np.asarray(A).shape[1]
+    if scaling == "uniform":
+        return choose_k(M, q), row_exponents(A), row_exponents(np.asarray(B).T)
+    if scaling == "fast":
+        return choose_k(M, 1), norm_exponents(A), norm_exponents(np.asarray(B).T)
+    if scaling == "accu":
+        kap, tA, tB = accu_exponents(A, B, M)[:3]
+        return kap, tA, tB
+    raise ValueError(f"unknown scaling {scaling!r}")
+
+
+# --------------------------------------------------------------------------
 # Whole method and the direct definition
 # --------------------------------------------------------------------------
 @dataclass
@@ -291,16 +461,13 @@ class Ozaki2Result:
     C3: np.ndarray = None      # C''' (object ints)
 
 
-def prepare(A: np.ndarray, B: np.ndarray, s: int, moduli=None):
+def prepare(A: np.ndarray, B: np.ndarray, s: int, moduli=None, scaling: str = "uniform"):
     """Steps 1-2: parameters, exponents and the truncated integer matrices."""
     A = np.asarray(A, dtype=np.float64)
     B = np.asarray(B, dtype=np.float64)
     moduli = list(moduli) if moduli is not None else greedy_moduli(s)
     cc = crt_constants(moduli)
-    q = A.shape[1]
-    k = choose_k(cc.M, q)
-    EA = row_exponents(A)
-    EB = row_exponents(B.T)
+    k, EA, EB = scaling_exponents(A, B, cc.M, scaling)
     d = scale_exponents(EA, k)
     e = scale_exponents(EB, k)
     Ap = scaled_trunc_matrix(A, d)
@@ -308,9 +475,10 @@ def prepare(A: np.ndarray, B: np.ndarray, s: int, moduli=None):
     return cc, k, EA, EB, d, e, Ap, Bp
 
 
-def ozaki2_dgemm(A: np.ndarray, B: np.ndarray, s: int, moduli=None, keep=True) -> Ozaki2Result:
-    """Algorithm 1 of [Ozaki II, §7], steps 1-6, in the pages' order."""
-    cc, k, EA, EB, d, e, Ap, Bp = prepare(A, B, s, moduli)
+def ozaki2_dgemm(A: np.ndarray, B: np.ndarray, s: int, moduli=None, keep=True,
+                 scaling: str = "uniform") -> Ozaki2Result:
+    """Algorithm 1 of [Ozaki II, §7], steps 1-6, in the pages' order (scaling: §5 or §9)."""
+    cc, k, EA, EB, d, e, Ap, Bp = prepare(A, B, s, moduli, scaling)
     Ares = residue_planes(Ap, cc.moduli)
     Bres = residue_planes(Bp, cc.moduli)
     Cres = residue_products(Ares, Bres, cc.moduli)
@@ -322,14 +490,15 @@ def ozaki2_dgemm(A: np.ndarray, B: np.ndarray, s: int, moduli=None, keep=True) -
     return r
 
 
-def direct_dgemm(A: np.ndarray, B: np.ndarray, s: int, moduli=None) -> np.ndarray:
+def direct_dgemm(A: np.ndarray, B: np.ndarray, s: int, moduli=None, scaling: str = "uniform") -> np.ndarray:
     """The same result from its definition: RN(2^-(d_i+e_j) * (A'B')_ij), exact integers."""
-    cc, k, EA, EB, d, e, Ap, Bp = prepare(A, B, s, moduli)
+    cc, k, EA, EB, d, e, Ap, Bp = prepare(A, B, s, moduli, scaling)
     C3 = np.dot(Ap.astype(object), Bp.astype(object))
     return unscale(C3, d, e, [x == "nan" for x in EA], [x == "nan" for x in EB])
 
 
-def direct_entries(A: np.ndarray, B: np.ndarray, s: int, rows, cols, moduli=None) -> np.ndarray:
+def direct_entries(A: np.ndarray, B: np.ndarray, s: int, rows, cols, moduli=None,
+                   scaling: str = "uniform") -> np.ndarray:
     """C_ij from the definition for selected (rows[p], cols[p]) pairs only.
 
     Uses the full row i of A and column j of B (their exponents span all of q),
@@ -339,11 +508,23 @@ def direct_entries(A: np.ndarray, B: np.ndarray, s: int, rows, cols, moduli=None
     B = np.asarray(B, dtype=np.float64)
     moduli = list(moduli) if moduli is not None else greedy_moduli(s)
     cc = crt_constants(moduli)
-    k = choose_k(cc.M, A.shape[1])
+    if scaling == "accu":
+        k, tA, tB = accu_exponents_sampled(A, B, cc.M, rows, cols)
+        rowexp = lambda i: tA[int(i)]
+        colexp = lambda j: tB[int(j)]
+    else:
+        if scaling == "uniform":
+            k, f = choose_k(cc.M, A.shape[1]), row_exponents
+        elif scaling == "fast":
+            k, f = choose_k(cc.M, 1), norm_exponents
+        else:
+            raise ValueError(f"unknown scaling {scaling!r}")
+        rowexp = lambda i: f(A[i : i + 1, :])[0]
+        colexp = lambda j: f(B[:, j : j + 1].T)[0]
     out = np.empty(len(rows), dtype=np.float64)
     for p, (i, j) in enumerate(zip(rows, cols)):
-        Ei = row_exponents(A[i : i + 1, :])[0]
-        Fj = row_exponents(B[:, j : j + 1].T)[0]
+        Ei = rowexp(i)
+        Fj = colexp(j)
         if Ei == "nan" or Fj == "nan":
             out[p] = np.nan
             continue
