@@ -13,7 +13,8 @@
 // residues go through shared memory to coalesced 16-byte stores of the uint8 plane.
 // This replaces the pages' block multiplication for k >= 2^17: the result is exact for
 // every k.  The same engine in exact mode (Scheme I) converts each chunk to INT32 and
-// adds it into the output.
+// adds it into the output, and in maximum mode (OS II-accu, one chunk holding the whole
+// k) reduces the product's rows and columns to their maxima.
 //
 // Kernel shape: clusters of two CTAs (cta_group::2), persistent over work units
 // (256 x 256 tile, modulus).  Each CTA loads its 128 rows of A and its 128 rows of B
@@ -167,6 +168,7 @@ struct PairSchedule {
 
 constexpr int kModeResidue = 0;  // Scheme II: C''_t = (A'_t B'_t) mod m_t, uint8 output
 constexpr int kModeExact = 1;    // Scheme I: exact INT32 slice products
+constexpr int kModeMax = 2;      // OS II-accu: row and column maxima of one exact product
 
 template <int MODE>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
@@ -347,7 +349,48 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     const int row_off = static_cast<int>(rank) * HALF_M;  // this CTA's rows of the tile
     uint32_t g = 0, eph = 0;
     bool ok = true;
-    if (MODE == kModeExact) {
+    if (MODE == kModeMax) {
+      // One chunk per unit (the launcher makes the whole k one chunk), so the accumulator
+      // holds the tile's exact non-negative integer sums; their FP32 bit patterns order
+      // like the values, so maxima are taken on the bits.
+      uint32_t* rho = static_cast<uint32_t*>(out_ptr);  // [mp] row maxima, then [np] column maxima
+      uint32_t* gamma = rho + mp;
+      for (int idx = 0; idx < sched.count() && ok; ++idx, ++g) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
+        const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        const uint32_t acc = g & 1;
+        if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+          ok = false;
+          if (lane == 0) record_timeout(abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
+        const int col0 = uc.tn * BN + half * 128;
+        uint32_t rmax = 0;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(taddr + cb * 32, v);
+          tmem_ld_wait();
+          if (cb == 3) {  // the whole tile is in registers: hand the accumulator back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
+          }
+          uint32_t mine = 0;  // maximum of column col0 + cb * 32 + lane over this warp's 32 rows
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            rmax = max(rmax, v[i]);
+            const uint32_t cm = __reduce_max_sync(0xFFFFFFFFu, v[i]);
+            if (lane == i) mine = cm;
+          }
+          atomicMax(gamma + col0 + cb * 32 + lane, mine);
+        }
+        atomicMax(rho + uc.tm * BM + row_off + row, rmax);
+      }
+    } else if (MODE == kModeExact) {
       int32_t* outp = static_cast<int32_t*>(out_ptr);
       for (int idx = 0; idx < sched.count() && ok; ++idx) {
         int u, kblk;
@@ -589,6 +632,19 @@ int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint1
 int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
                       const uint16_t* A_planes, const uint16_t* B_planes, int32_t* out, cudaStream_t stream) {
   return launch_gemm<kModeExact>(mp, np, kp, a_planes, b_planes, c, A_planes, B_planes, out, stream);
+}
+
+int launch_bound_gemm(int mp, int np, int kp, const uint16_t* A_plane, const uint16_t* B_plane, uint32_t* maxes,
+                      cudaStream_t stream) {
+  GemmConsts c{};
+  c.s = 1;
+  c.kb_per_chunk = kp / gemm::BK;  // the whole k in one chunk: the caller keeps q 4^b <= 2^24
+  c.kb_per_block = c.kb_per_chunk;
+  c.a_plane[0] = 0;
+  c.b_plane[0] = 0;
+  if (cudaMemsetAsync(maxes, 0, sizeof(uint32_t) * (static_cast<size_t>(mp) + np), stream) != cudaSuccess)
+    return OZ_ECUDA;
+  return launch_gemm<kModeMax>(mp, np, kp, 1, 1, c, A_plane, B_plane, maxes, stream);
 }
 
 }  // namespace oz

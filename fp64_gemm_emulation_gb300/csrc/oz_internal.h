@@ -58,6 +58,7 @@ struct GemmConsts {
 // Host-side helpers (ozaki_host.cu).
 int fill_split_consts(int s, long long k_inner, SplitConsts* out);
 int fill_crt_consts(int s, long long k_inner, CrtConsts* out);
+int half_range_log2(int s);  // L = floor(log2(M/2 - 1)) for the first s moduli; -1 on error
 
 // Kernel launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
@@ -69,6 +70,16 @@ int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint1
                         const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
 int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
                       const uint16_t* A_planes, const uint16_t* B_planes, int32_t* out, cudaStream_t stream);
+int launch_bound_gemm(int mp, int np, int kp, const uint16_t* A_plane, const uint16_t* B_plane, uint32_t* maxes,
+                      cudaStream_t stream);
+cudaError_t launch_norm_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                                  int32_t* rowexp, int32_t* colexp, unsigned long long* Srow,
+                                  unsigned long long* Scol, cudaStream_t stream);
+cudaError_t launch_magnitudes(int rows, int k, const double* X, long long row_stride, long long k_stride,
+                              const int32_t* exps, int b, uint16_t* plane, int rows_padded, int kp,
+                              cudaStream_t stream);
+cudaError_t launch_accu_finalize(int count, int32_t* exps, const uint32_t* maxes, int L, int kappa, int b,
+                                 cudaStream_t stream);
 cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
                        const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream);
 cudaError_t launch_fill_zero(int m, int n, double* C, int ldc, cudaStream_t stream);

@@ -180,6 +180,15 @@ int fill_crt_consts(int s, long long k_inner, CrtConsts* out) {
   return OZ_OK;
 }
 
+int half_range_log2(int s) {
+  Params p;
+  if (make_params(s, &p)) return -1;
+  const Big lim = big_sub_small(p.M, 2);  // 2^(L+1) <= M - 2 < 2^(L+2)
+  for (int i = kBigLimbs - 1; i >= 0; --i)
+    if (lim.w[i]) return 32 * i + (31 - __builtin_clz(lim.w[i])) - 1;
+  return -1;
+}
+
 }  // namespace oz
 
 using namespace oz;
@@ -268,6 +277,58 @@ GemmConsts make_gemm_consts(const SplitConsts& sc) {
   return g;
 }
 
+bool valid_scaling(int scaling) {
+  return scaling == OZ_SCALE_UNIFORM || scaling == OZ_SCALE_FAST || scaling == OZ_SCALE_ACCU;
+}
+
+// The inner dimension whose k_A the split and the CRT use: the uniform estimate bounds
+// c_max by q 2^(k_A + k_B); fast and accu bound it by 2^(2 kappa), the k_A of q = 1.
+long long scaling_q(int scaling, long long k) { return scaling == OZ_SCALE_UNIFORM ? k : 1; }
+
+// OS II-accu: the largest b in [0, 7] with q 4^b <= 2^24; -1 when q > 2^24.
+int accu_bits(long long q) {
+  if (q < 1 || q > (1LL << 24)) return -1;
+  int b = 0;
+  while (b < 7 && (q << (2 * b + 2)) <= (1LL << 24)) ++b;
+  return b;
+}
+
+// Workspace of the exponent step (scaling modes other than uniform).
+struct ExpLayout {
+  size_t off_S_row, off_S_col;           // fast: uint64 [m], [n]
+  size_t off_Ahat, off_Bhat, off_maxes;  // accu: bf16 [Mp][Kp], [Np][Kp]; uint32 [Mp + Np]
+  size_t total;
+};
+
+ExpLayout make_exp_layout(int m, int n, int k, int scaling) {
+  ExpLayout E{};
+  const size_t mp = static_cast<size_t>(roundup(m, kPadM)), np = static_cast<size_t>(roundup(n, kPadN)),
+               kp = static_cast<size_t>(roundup(k, kPadK));
+  size_t off = 0;
+  if (scaling == OZ_SCALE_FAST) {
+    E.off_S_row = off;
+    off = align256(off + sizeof(unsigned long long) * static_cast<size_t>(m));
+    E.off_S_col = off;
+    off = align256(off + sizeof(unsigned long long) * static_cast<size_t>(n));
+  } else if (scaling == OZ_SCALE_ACCU) {
+    E.off_Ahat = off;
+    off = align256(off + sizeof(uint16_t) * mp * kp);
+    E.off_Bhat = off;
+    off = align256(off + sizeof(uint16_t) * np * kp);
+    E.off_maxes = off;
+    off = align256(off + sizeof(uint32_t) * (mp + np));
+  }
+  E.total = off;
+  return E;
+}
+
+// Whole-call workspace: the exponent step's scratch lives where C_res will go (it is
+// consumed before the split, and C_res is written only by the GEMM after it).
+size_t total_bytes_ex(const Layout& L, int m, int n, int k, int scaling) {
+  const size_t e = L.off_C + make_exp_layout(m, n, k, scaling).total;
+  return e > L.total ? align256(e) : L.total;
+}
+
 }  // namespace
 
 extern "C" {
@@ -308,15 +369,72 @@ int ozaki2_exponents(int m, int n, int k, const double* A, int lda, const double
   return cuda_rc(launch_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream));
 }
 
+int ozaki2_scaling_k(int num_moduli, long long k_inner, int scaling, int* k_out) {
+  if (!valid_scaling(scaling)) return OZ_EINVAL;
+  if (scaling == OZ_SCALE_ACCU && accu_bits(k_inner) < 0) return OZ_EINVAL;
+  if (!k_out || k_inner < 1) return OZ_EINVAL;
+  return ozaki2_choose_k(num_moduli, scaling_q(scaling, k_inner), k_out);
+}
+
+size_t ozaki2_exponents_workspace_bytes(int m, int n, int k, int scaling) {
+  if (m < 0 || n < 0 || k < 0 || !valid_scaling(scaling)) return 0;
+  return make_exp_layout(m, n, k, scaling).total;
+}
+
+int ozaki2_exponents_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
+                        int scaling, int32_t* rowexp, int32_t* colexp, void* workspace, size_t ws_bytes,
+                        cudaStream_t stream) {
+  if (!valid_scaling(scaling) || num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (scaling == OZ_SCALE_UNIFORM) return ozaki2_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream);
+  if (m < 0 || n < 0 || k < 0) return OZ_EINVAL;
+  if ((A && (lda < (m > 1 ? m : 1) || !rowexp)) || (B && (ldb < (k > 1 ? k : 1) || !colexp))) return OZ_EINVAL;
+  if (scaling == OZ_SCALE_ACCU && (!A || !B || (k > 0 && accu_bits(k) < 0))) return OZ_EINVAL;
+  const ExpLayout E = make_exp_layout(m, n, k, scaling);
+  if (E.total && (!workspace || ws_bytes < E.total || (reinterpret_cast<uintptr_t>(workspace) & 255)))
+    return OZ_ENOMEM;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (scaling == OZ_SCALE_FAST)
+    return cuda_rc(launch_norm_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp,
+                                         reinterpret_cast<unsigned long long*>(ws + E.off_S_row),
+                                         reinterpret_cast<unsigned long long*>(ws + E.off_S_col), stream));
+  // OS II-accu: maxima exponents, rounded-up magnitudes, their exact product's row and
+  // column maxima, then the exponents of the scaling.
+  int rc = cuda_rc(launch_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream));
+  if (rc || k == 0 || m == 0 || n == 0) return rc;
+  Params p;
+  if ((rc = make_params(num_moduli, &p))) return rc;
+  const int kappa = oz::choose_k(p.M, 1);
+  const int L = half_range_log2(num_moduli);
+  const int b = accu_bits(k);
+  if (kappa < 1 || L < 0 || b < 0) return OZ_EINVAL;
+  const int mp = static_cast<int>(roundup(m, kPadM)), np = static_cast<int>(roundup(n, kPadN)),
+            kp = static_cast<int>(roundup(k, kPadK));
+  uint16_t* Ahat = reinterpret_cast<uint16_t*>(ws + E.off_Ahat);
+  uint16_t* Bhat = reinterpret_cast<uint16_t*>(ws + E.off_Bhat);
+  uint32_t* maxes = reinterpret_cast<uint32_t*>(ws + E.off_maxes);
+  if ((rc = cuda_rc(launch_magnitudes(m, k, A, 1, lda, rowexp, b, Ahat, mp, kp, stream)))) return rc;
+  if ((rc = cuda_rc(launch_magnitudes(n, k, B, ldb, 1, colexp, b, Bhat, np, kp, stream)))) return rc;
+  if ((rc = launch_bound_gemm(mp, np, kp, Ahat, Bhat, maxes, stream))) return rc;
+  if ((rc = cuda_rc(launch_accu_finalize(m, rowexp, maxes, L, kappa, b, stream)))) return rc;
+  return cuda_rc(launch_accu_finalize(n, colexp, maxes + mp, L, kappa, b, stream));
+}
+
 int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
                  const int32_t* rowexp, const int32_t* colexp, uint16_t* A_planes, uint16_t* B_planes,
                  cudaStream_t stream) {
-  if (m < 0 || n < 0 || k < 1) return OZ_EINVAL;
+  return ozaki2_split_ex(m, n, k, A, lda, B, ldb, num_moduli, OZ_SCALE_UNIFORM, rowexp, colexp, A_planes, B_planes,
+                         stream);
+}
+
+int ozaki2_split_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
+                    int scaling, const int32_t* rowexp, const int32_t* colexp, uint16_t* A_planes,
+                    uint16_t* B_planes, cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1 || !valid_scaling(scaling)) return OZ_EINVAL;
   if ((A && (lda < (m > 1 ? m : 1) || !rowexp || !A_planes)) || (B && (ldb < (k > 1 ? k : 1) || !colexp || !B_planes)))
     return OZ_EINVAL;
   if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
   SplitConsts sc;
-  int rc = fill_split_consts(num_moduli, k, &sc);
+  int rc = fill_split_consts(num_moduli, scaling_q(scaling, k), &sc);
   if (rc) return rc;
   const int mp = static_cast<int>(roundup(m, kPadM)), np = static_cast<int>(roundup(n, kPadN)),
             kp = static_cast<int>(roundup(k, kPadK));
@@ -336,8 +454,8 @@ int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_p
   if (m < 0 || n < 0 || k < 1 || !A_planes || !B_planes || !C_res) return OZ_EINVAL;
   if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
   if (m == 0 || n == 0) return OZ_OK;
-  SplitConsts sc;
-  const int rc = fill_split_consts(num_moduli, k, &sc);
+  SplitConsts sc;  // only the moduli are used: no dependence on k_A or the scaling mode
+  const int rc = fill_split_consts(num_moduli, 1, &sc);
   if (rc) return rc;
   return launch_residue_gemm(static_cast<int>(roundup(m, kPadM)), static_cast<int>(roundup(n, kPadN)),
                              static_cast<int>(roundup(k, kPadK)), make_gemm_consts(sc), A_planes, B_planes, C_res,
@@ -346,10 +464,15 @@ int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_p
 
 int ozaki2_crt(int m, int n, int k, int num_moduli, const uint8_t* C_res, const int32_t* rowexp,
                const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
+  return ozaki2_crt_ex(m, n, k, num_moduli, OZ_SCALE_UNIFORM, C_res, rowexp, colexp, C, ldc, stream);
+}
+
+int ozaki2_crt_ex(int m, int n, int k, int num_moduli, int scaling, const uint8_t* C_res, const int32_t* rowexp,
+                  const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
   if (m < 0 || n < 0 || k < 1 || !C_res || !rowexp || !colexp || !C || ldc < (m > 1 ? m : 1)) return OZ_EINVAL;
-  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI || !valid_scaling(scaling)) return OZ_EINVAL;
   CrtConsts cc;
-  const int rc = fill_crt_consts(num_moduli, k, &cc);
+  const int rc = fill_crt_consts(num_moduli, scaling_q(scaling, k), &cc);
   if (rc) return rc;
   return cuda_rc(launch_crt(m, n, static_cast<int>(roundup(m, kPadM)), static_cast<int>(roundup(n, kPadN)), cc,
                             C_res, rowexp, colexp, C, ldc, stream));
@@ -381,6 +504,66 @@ int ozaki2_dgemm_ws(int m, int n, int k, const double* A, int lda, const double*
   if ((rc = ozaki2_split(m, n, k, A, lda, B, ldb, num_moduli, rowexp, colexp, Ap, Bp, stream))) return rc;
   if ((rc = ozaki2_residue_gemm(m, n, k, num_moduli, Ap, Bp, Cr, stream))) return rc;
   return ozaki2_crt(m, n, k, num_moduli, Cr, rowexp, colexp, C, ldc, stream);
+}
+
+size_t ozaki2_workspace_bytes_ex(int m, int n, int k, int num_moduli, int scaling) {
+  if (m < 0 || n < 0 || k < 0 || num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI || !valid_scaling(scaling))
+    return 0;
+  return total_bytes_ex(make_layout(m, n, k, num_moduli), m, n, k, scaling);
+}
+
+int ozaki2_dgemm_ex_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                       int num_moduli, int scaling, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_dims(m, n, k, lda, ldb, ldc);
+  if (rc) return rc;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI || !valid_scaling(scaling)) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (!C) return OZ_EINVAL;
+  if (k == 0) return cuda_rc(launch_fill_zero(m, n, C, ldc, stream));
+  if (!A || !B) return OZ_EINVAL;
+  {
+    int kA;
+    if ((rc = ozaki2_scaling_k(num_moduli, k, scaling, &kA))) return rc;
+  }
+  const Layout L = make_layout(m, n, k, num_moduli);
+  const size_t total = total_bytes_ex(L, m, n, k, scaling);
+  if (!workspace || ws_bytes < total || (reinterpret_cast<uintptr_t>(workspace) & 255)) return OZ_ENOMEM;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* rowexp = reinterpret_cast<int32_t*>(ws + L.off_rowexp);
+  int32_t* colexp = reinterpret_cast<int32_t*>(ws + L.off_colexp);
+  uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + L.off_A);
+  uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + L.off_B);
+  uint8_t* Cr = ws + L.off_C;
+  if ((rc = ozaki2_exponents_ex(m, n, k, A, lda, B, ldb, num_moduli, scaling, rowexp, colexp, Cr, total - L.off_C,
+                                stream)))
+    return rc;
+  if ((rc = ozaki2_split_ex(m, n, k, A, lda, B, ldb, num_moduli, scaling, rowexp, colexp, Ap, Bp, stream))) return rc;
+  if ((rc = ozaki2_residue_gemm(m, n, k, num_moduli, Ap, Bp, Cr, stream))) return rc;
+  return ozaki2_crt_ex(m, n, k, num_moduli, scaling, Cr, rowexp, colexp, C, ldc, stream);
+}
+
+int ozaki2_dgemm_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,
+                    int num_moduli, int scaling, cudaStream_t stream) {
+  int rc = check_dims(m, n, k, lda, ldb, ldc);
+  if (rc) return rc;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI || !valid_scaling(scaling)) return OZ_EINVAL;
+  if (m == 0 || n == 0) return OZ_OK;
+  if (k == 0) return C ? cuda_rc(launch_fill_zero(m, n, C, ldc, stream)) : OZ_EINVAL;
+  {
+    int kA;
+    if ((rc = ozaki2_scaling_k(num_moduli, k, scaling, &kA))) return rc;
+  }
+  const size_t bytes = ozaki2_workspace_bytes_ex(m, n, k, num_moduli, scaling);
+  keep_default_pool_cached();
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return OZ_ENOMEM;
+  }
+  rc = ozaki2_dgemm_ex_ws(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, scaling, ws, bytes, stream);
+  const cudaError_t e = cudaFreeAsync(ws, stream);
+  if (rc == OZ_OK && e != cudaSuccess) rc = OZ_ECUDA;
+  return rc;
 }
 
 int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb, double* C, int ldc,

@@ -24,6 +24,8 @@ OZ_EXP_EMPTY = np.int32(np.uint32(0x80808080).view(np.int32))
 OZ_EXP_NONFINITE = np.int32(0x7FFFFFFF)
 PAD_M, PAD_N, PAD_K = 256, 256, 64
 OZ_NOALLOC_SCRATCH_BYTES = 64 << 20
+OZ_SCALE_UNIFORM, OZ_SCALE_FAST, OZ_SCALE_ACCU = 0, 1, 2
+SCALINGS = {"uniform": OZ_SCALE_UNIFORM, "fast": OZ_SCALE_FAST, "accu": OZ_SCALE_ACCU}
 
 
 class OzakiError(RuntimeError):
@@ -50,6 +52,14 @@ def _load():
         "ozaki2_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
         "ozaki2_dgemm_host": (I, [I, I, I, P, I, P, I, P, I, I]),
         "ozaki2_dgemm_noalloc": (I, [I, I, I, P, I, P, I, P, I, I, P]),
+        "ozaki2_scaling_k": (I, [I, L, I, P]),
+        "ozaki2_exponents_workspace_bytes": (S, [I, I, I, I]),
+        "ozaki2_exponents_ex": (I, [I, I, I, P, I, P, I, I, I, P, P, P, S, P]),
+        "ozaki2_split_ex": (I, [I, I, I, P, I, P, I, I, I, P, P, P, P, P]),
+        "ozaki2_crt_ex": (I, [I, I, I, I, I, P, P, P, P, I, P]),
+        "ozaki2_workspace_bytes_ex": (S, [I, I, I, I, I]),
+        "ozaki2_dgemm_ex_ws": (I, [I, I, I, P, I, P, I, P, I, I, I, P, S, P]),
+        "ozaki2_dgemm_ex": (I, [I, I, I, P, I, P, I, P, I, I, I, P]),
         "ozaki1_beta": (I, [L, P]),
         "ozaki1_split_scratch_bytes": (S, [I, I, I]),
         "ozaki1_workspace_bytes": (S, [I, I, I, I]),
@@ -231,6 +241,92 @@ def ozaki2_dgemm_host(A: np.ndarray, B: np.ndarray, num_moduli: int = 14, C: np.
 def ozaki2_dgemm_host_ptr(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli):
     """Raw-pointer form of ozaki2_dgemm_host (host pointers, e.g. pinned torch tensors)."""
     _check(_lib.ozaki2_dgemm_host(m, n, k, a_ptr, lda, b_ptr, ldb, c_ptr, ldc, num_moduli), "ozaki2_dgemm_host")
+
+
+# ------------------------------------------------------------------ range estimation modes
+def _scaling(scaling) -> int:
+    return SCALINGS[scaling] if isinstance(scaling, str) else int(scaling)
+
+
+def ozaki2_scaling_k(num_moduli: int, k_inner: int, scaling="uniform") -> int:
+    k = ctypes.c_int()
+    _check(_lib.ozaki2_scaling_k(num_moduli, k_inner, _scaling(scaling), ctypes.byref(k)), "ozaki2_scaling_k")
+    return k.value
+
+
+def ozaki2_exponents_workspace_bytes(m: int, n: int, k: int, scaling="uniform") -> int:
+    return int(_lib.ozaki2_exponents_workspace_bytes(m, n, k, _scaling(scaling)))
+
+
+def ozaki2_workspace_bytes_ex(m: int, n: int, k: int, num_moduli: int, scaling="uniform") -> int:
+    return int(_lib.ozaki2_workspace_bytes_ex(m, n, k, num_moduli, _scaling(scaling)))
+
+
+def ozaki2_exponents_ex(A, B, num_moduli: int, scaling="uniform", stream=None):
+    """Step a1 in a scaling mode: (rowexp[m], colexp[n]) int32 tensors."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    sc = _scaling(scaling)
+    rowexp = torch.empty(m, dtype=torch.int32, device=A.device)
+    colexp = torch.empty(n, dtype=torch.int32, device=A.device)
+    nbytes = ozaki2_exponents_workspace_bytes(m, n, k, sc)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=A.device)
+    _check(_lib.ozaki2_exponents_ex(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_moduli, sc, _ptr(rowexp),
+                                    _ptr(colexp), _ptr(ws), nbytes, _stream(stream)), "ozaki2_exponents_ex")
+    return rowexp, colexp
+
+
+def ozaki2_split_ex(A, B, num_moduli: int, rowexp, colexp, scaling="uniform", stream=None):
+    """Step a2 for exponents of a scaling mode (planes as in ozaki2_split)."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    Ap = torch.empty((num_moduli, mp, kp), dtype=torch.int16, device=A.device)
+    Bp = torch.empty((num_moduli, np_, kp), dtype=torch.int16, device=A.device)
+    _check(_lib.ozaki2_split_ex(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_moduli, _scaling(scaling),
+                                _ptr(rowexp), _ptr(colexp), _ptr(Ap), _ptr(Bp), _stream(stream)), "ozaki2_split_ex")
+    return Ap, Bp
+
+
+def ozaki2_crt_ex(m: int, n: int, k: int, num_moduli: int, C_res, rowexp, colexp, scaling="uniform", C=None,
+                  stream=None):
+    """Steps a5+a6 for exponents of a scaling mode."""
+    import torch
+
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=C_res.device).t()
+    _check(_lib.ozaki2_crt_ex(m, n, k, num_moduli, _scaling(scaling), _ptr(C_res), _ptr(rowexp), _ptr(colexp),
+                              _ptr(C), _ld(C), _stream(stream)), "ozaki2_crt_ex")
+    return C
+
+
+def ozaki2_dgemm_ex(A, B, num_moduli: int = 14, scaling="uniform", C=None, workspace=None, stream=None):
+    """C = A B by Ozaki Scheme II in a scaling mode ("uniform", "fast", "accu");
+    with ``workspace`` (uint8 tensor of ozaki2_workspace_bytes_ex bytes) the _ws form."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    sc = _scaling(scaling)
+    if workspace is None:
+        rc = _lib.ozaki2_dgemm_ex(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli, sc,
+                                  _stream(stream))
+    else:
+        rc = _lib.ozaki2_dgemm_ex_ws(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_moduli, sc,
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "ozaki2_dgemm_ex")
+    return C
+
+
+def ozaki2_dgemm_ex_ws(A, B, num_moduli: int, scaling, workspace, C=None, stream=None):
+    """C = A B in a scaling mode with a caller-owned workspace (ozaki2_workspace_bytes_ex bytes)."""
+    return ozaki2_dgemm_ex(A, B, num_moduli, scaling, C=C, workspace=workspace, stream=stream)
 
 
 # ------------------------------------------------------------------ Scheme I

@@ -23,6 +23,7 @@ def main():
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--scheme", type=int, choices=[1, 2], default=2)
     ap.add_argument("--slices", type=int, default=7)
+    ap.add_argument("--scaling", choices=["uniform", "fast", "accu"], default="uniform")
     a = ap.parse_args()
     if a.scheme == 1:
         return run_scheme1(a)
@@ -43,18 +44,21 @@ def main():
     Ap = torch.empty((s, mp, kp), dtype=torch.int16, device="cuda")
     Bp = torch.empty((s, np_, kp), dtype=torch.int16, device="cuda")
     Cr = torch.empty((s, np_, mp), dtype=torch.uint8, device="cuda")
+    sc = oz.SCALINGS[a.scaling]
+    nb = oz.ozaki2_exponents_workspace_bytes(m, n, k, sc)
+    ews = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
     lib, st = oz._lib, torch.cuda.current_stream().cuda_stream
     p = lambda t: t.data_ptr()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for _ in range(a.reps):
         ev[0].record()
-        rc = lib.ozaki2_exponents(m, n, k, p(dA), m, p(dB), k, p(rowexp), p(colexp), st)
+        rc = lib.ozaki2_exponents_ex(m, n, k, p(dA), m, p(dB), k, s, sc, p(rowexp), p(colexp), p(ews), nb, st)
         ev[1].record()
-        rc |= lib.ozaki2_split(m, n, k, p(dA), m, p(dB), k, s, p(rowexp), p(colexp), p(Ap), p(Bp), st)
+        rc |= lib.ozaki2_split_ex(m, n, k, p(dA), m, p(dB), k, s, sc, p(rowexp), p(colexp), p(Ap), p(Bp), st)
         ev[2].record()
         rc |= lib.ozaki2_residue_gemm(m, n, k, s, p(Ap), p(Bp), p(Cr), st)
         ev[3].record()
-        rc |= lib.ozaki2_crt(m, n, k, s, p(Cr), p(rowexp), p(colexp), p(dC), m, st)
+        rc |= lib.ozaki2_crt_ex(m, n, k, s, sc, p(Cr), p(rowexp), p(colexp), p(dC), m, st)
         ev[4].record()
         if rc:
             raise SystemExit(f"ozaki call failed: {rc}")
@@ -62,7 +66,7 @@ def main():
     status = oz.ozaki_get_device_status()
     names = ["exponents", "split", "residue_gemm", "crt"]
     t = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
-    print(f"{m}x{n}x{k} s={s}: " + ", ".join(f"{nm} {x:.3f} ms" for nm, x in zip(names, t))
+    print(f"{m}x{n}x{k} s={s} {a.scaling}: " + ", ".join(f"{nm} {x:.3f} ms" for nm, x in zip(names, t))
           + f"; gemm {s * 2.0 * m * n * k / (t[2] * 1e-3) / 1e12:.1f} TFLOP/s; status {status}")
     if status:
         raise SystemExit(1)

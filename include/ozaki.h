@@ -134,6 +134,63 @@ int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
 int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                       double* C, int ldc, int num_moduli);
 
+/* ---------------------------------------------------------------- Scheme II range estimation */
+
+/* How the scaling exponents keep the CRT result unique ([Ozaki II] sections 5 and 9):
+ * every mode guarantees max_ij (|A'||B'|)_ij <= M/2 - 1 and writes exponent codes t
+ * with d_i = k - t_i (row i of A) and e_j = k - t_j (column j of B), where k is the
+ * value ozaki2_scaling_k returns.  OZ_EXP_EMPTY / OZ_EXP_NONFINITE keep their meaning.
+ *  OZ_SCALE_UNIFORM: c_max = q 2^(k_A + k_B); t_i = ceil(log2 max_j |a_ij|), k = k_A
+ *    (the mode of every entry point without _ex).
+ *  OZ_SCALE_FAST (OS II-fast, Cauchy-Schwarz): 2^t_i >= ||a_i,:||_2, computed from
+ *    exact integers (c_l = ceil(log2 |a_il|), G = 16, S = sum_l max(1, 4^(c_l - c_max + G)),
+ *    t = c_max - G + ceil(ceil(log2 S) / 2)); k = kappa = the largest k with
+ *    2^(2k) <= M/2 - 1.
+ *  OZ_SCALE_ACCU (OS II-accu, a low-precision product): magnitudes rounded up to b bits
+ *    of each row's range (b = the largest integer <= 7 with q 4^b <= 2^24), their
+ *    exact product C^ on the tensor cores (one bf16 GEMM), rho_i = max(1, max_j C^_ij),
+ *    gamma_j likewise, L = floor(log2(M/2 - 1)),
+ *    t_i = kappa - floor((L - ceil(log2 rho_i)) / 2) + ceil(log2 max_j |a_ij|) - b.
+ *    Needs k <= 2^24 (OZ_EINVAL otherwise). */
+#define OZ_SCALE_UNIFORM 0
+#define OZ_SCALE_FAST 1
+#define OZ_SCALE_ACCU 2
+
+/* k of the scaling mode for num_moduli and the inner dimension k_inner (host only).
+ * OZ_ERANGE as ozaki2_choose_k; OZ_EINVAL for an unknown mode or, for OZ_SCALE_ACCU,
+ * k_inner > 2^24. */
+int ozaki2_scaling_k(int num_moduli, long long k_inner, int scaling, int* k_out);
+
+/* Device scratch bytes ozaki2_exponents_ex needs: 0 (uniform), 8(m + n) (fast),
+ * 2 Kp (Mp + Np) + 4 (Mp + Np) plus alignment (accu). */
+size_t ozaki2_exponents_workspace_bytes(int m, int n, int k, int scaling);
+
+/* Step a1 in a given scaling mode: writes rowexp[m] (if A) and colexp[n] (if B).
+ * OZ_SCALE_ACCU needs both operands.  workspace: device memory of at least
+ * ozaki2_exponents_workspace_bytes bytes, 256-byte aligned (OZ_ENOMEM otherwise; may
+ * be null when that is 0).  num_moduli fixes M (unused by uniform and fast). */
+int ozaki2_exponents_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                        int num_moduli, int scaling, int32_t* rowexp, int32_t* colexp,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Steps a2 and a5 + a6 for exponents of a given scaling mode (same layouts and errors
+ * as ozaki2_split and ozaki2_crt, which are these with OZ_SCALE_UNIFORM). */
+int ozaki2_split_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    int num_moduli, int scaling, const int32_t* rowexp, const int32_t* colexp,
+                    uint16_t* A_planes, uint16_t* B_planes, cudaStream_t stream);
+int ozaki2_crt_ex(int m, int n, int k, int num_moduli, int scaling, const uint8_t* C_res,
+                  const int32_t* rowexp, const int32_t* colexp, double* C, int ldc,
+                  cudaStream_t stream);
+
+/* The whole path in a given scaling mode: workspace bytes, caller-owned workspace,
+ * stream-ordered allocation (as ozaki2_dgemm_ws / ozaki2_dgemm). */
+size_t ozaki2_workspace_bytes_ex(int m, int n, int k, int num_moduli, int scaling);
+int ozaki2_dgemm_ex_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                       double* C, int ldc, int num_moduli, int scaling, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+int ozaki2_dgemm_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    double* C, int ldc, int num_moduli, int scaling, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- Scheme I (comparison path) */
 
 /* Scheme I ([Ozaki notes]: RN split of Uchino et al., the triangular integer products

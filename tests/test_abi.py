@@ -119,3 +119,59 @@ def test_ozaki1_workspace(oz):
     assert oz.ozaki1_workspace_bytes(300, 520, 2100, 0) == 0
     assert oz.ozaki1_workspace_bytes(300, 520, 2100, 21) == 0
     assert oz.ozaki1_split_scratch_bytes(300, 520, 2100) >= 8 * (300 * 2100 + 2100 * 520)
+
+
+# ------------------------------------------------------------------ range estimation modes
+@pytest.mark.parametrize("s", [2, 3, 8, 14, 16, 20])
+@pytest.mark.parametrize("q", [1, 256, 1025, 16384, 262144, 2**24, 2**24 + 1, 2**30])
+@pytest.mark.parametrize("scaling", ["uniform", "fast", "accu"])
+def test_scaling_k_matches_the_oracle(oz, s, q, scaling):
+    M = O.crt_constants(O.greedy_moduli(s)).M
+    if scaling == "accu" and q > 2**24:
+        with pytest.raises(oz.OzakiError) as e:
+            oz.ozaki2_scaling_k(s, q, scaling)
+        assert e.value.code == oz.OZ_EINVAL
+        return
+    try:
+        want = O.choose_k(M, q if scaling == "uniform" else 1)
+    except ValueError:
+        want = None
+    if want is None or want < 1:
+        with pytest.raises(oz.OzakiError):
+            oz.ozaki2_scaling_k(s, q, scaling)
+    else:
+        assert oz.ozaki2_scaling_k(s, q, scaling) == want
+        if scaling != "uniform":
+            assert want == O.half_range_log2(M) // 2
+
+
+def test_scaling_workspace_sizes(oz):
+    m, n, k = 300, 520, 2100
+    mp, np_, kp = oz.ozaki2_plane_dims(m, n, k)
+    assert oz.ozaki2_exponents_workspace_bytes(m, n, k, "uniform") == 0
+    assert oz.ozaki2_exponents_workspace_bytes(m, n, k, "fast") >= 8 * (m + n)
+    assert oz.ozaki2_exponents_workspace_bytes(m, n, k, "accu") >= 2 * kp * (mp + np_) + 4 * (mp + np_)
+    base = oz.ozaki2_workspace_bytes(m, n, k, 14)
+    assert oz.ozaki2_workspace_bytes_ex(m, n, k, 14, "uniform") == base
+    assert oz.ozaki2_workspace_bytes_ex(m, n, k, 14, "fast") >= base
+    # the exponent scratch overlays the C_res region: the total grows only when it is larger
+    tall = oz.ozaki2_workspace_bytes_ex(256, 256, 262144, 14, "accu")
+    assert tall >= oz.ozaki2_workspace_bytes(256, 256, 262144, 14)
+    assert oz.ozaki2_workspace_bytes_ex(m, n, k, 14, 7) == 0
+
+
+def test_scaling_argument_errors(oz):
+    lib = oz._lib
+    null = None
+    # unknown scaling mode
+    assert lib.ozaki2_dgemm_ex(8, 4, 4, 1, 8, 1, 4, 1, 8, 14, 3, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_ex(8, 4, 4, 1, 8, 1, 4, 1, 8, 14, -1, null) == oz.OZ_EINVAL
+    # accu needs k <= 2^24 and both operands
+    assert lib.ozaki2_dgemm_ex_ws(8, 8, 2**24 + 1, 1, 8, 1, 2**24 + 1, 1, 8, 14, 2, 256, 1 << 40, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_exponents_ex(8, 8, 8, 1, 8, null, 8, 14, 2, 1, 1, 256, 1 << 30, null) == oz.OZ_EINVAL
+    # fast / accu scratch too small
+    assert lib.ozaki2_exponents_ex(8, 8, 8, 1, 8, 1, 8, 14, 1, 1, 1, 256, 8, null) == oz.OZ_ENOMEM
+    assert lib.ozaki2_dgemm_ex_ws(8, 8, 8, 1, 8, 1, 8, 1, 8, 14, 2, 256, 16, null) == oz.OZ_ENOMEM
+    # split / crt reject an unknown mode
+    assert lib.ozaki2_split_ex(8, 8, 8, 1, 8, 1, 8, 14, 5, 1, 1, 1, 1, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_crt_ex(8, 8, 8, 14, 5, 1, 1, 1, 1, 8, null) == oz.OZ_EINVAL
