@@ -321,12 +321,46 @@ def run_ours(args, world, rank, local):
         "gemm_frac_of_b200_int8_spec_4500": achieved / 4500.0,
     }
 
+    # ---- the range-estimation variants ([Ozaki II, §9]) on the same workload
+    variants = {}
+    if not args.no_variants:
+        for name, sc in (("fast", oz.OZ_SCALE_FAST), ("accu", oz.OZ_SCALE_ACCU)):
+            nb = oz.ozaki2_exponents_workspace_bytes(M, N, K, sc)
+            ews = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+
+            def vstep(ev=None):
+                if ev:
+                    ev[0].record(stream)
+                rc = lib.ozaki2_exponents_ex(M, N, K, ptr(dA), M, ptr(dB), K, S, sc, ptr(rowexp), ptr(colexp),
+                                             ptr(ews), nb, sh)
+                if ev:
+                    ev[1].record(stream)
+                rc |= lib.ozaki2_split_ex(M, N, K, ptr(dA), M, ptr(dB), K, S, sc, ptr(rowexp), ptr(colexp), ptr(Ap),
+                                          ptr(Bp), sh)
+                rc |= lib.ozaki2_residue_gemm(M, N, K, S, ptr(Ap), ptr(Bp), ptr(Cr), sh)
+                rc |= lib.ozaki2_crt_ex(M, N, K, S, sc, ptr(Cr), ptr(rowexp), ptr(colexp), ptr(dC), M, sh)
+                if ev:
+                    ev[2].record(stream)
+                if rc:
+                    raise RuntimeError(f"ozaki {name} call failed: {rc}")
+
+            vstep()
+            vev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(3)]
+            for e in vev:
+                vstep(e)
+            torch.cuda.synchronize(device)
+            step_ms = float(np.mean([e[0].elapsed_time(e[2]) for e in vev]))
+            variants[name] = {"ms_per_step": step_ms, "value": flops / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+                              "exponents_ms": float(np.mean([e[0].elapsed_time(e[1]) for e in vev])), "steps": 3}
+            del ews
+
     # ---- end to end through the C ABI with pinned HOST buffers
     hA = torch.from_numpy(A_np.T.copy()).pin_memory()   # column-major A as a (k, m) row-major block
     hB = torch.from_numpy(B_np.T.copy()).pin_memory()
     hC = torch.empty((N, M), dtype=torch.float64).pin_memory()
     e2e_steps = args.steps
-    oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)  # warm-up
+    for _ in range(args.warmup):  # the same W warm-up steps as the device-resident loop
+        oz.ozaki2_dgemm_host_ptr(M, N, K, hA.data_ptr(), M, hB.data_ptr(), K, hC.data_ptr(), M, S)
     e2e_clocks = ClockSampler(local, "_e2e")
     e2e_clocks.start()
     time.sleep(0.3)
@@ -373,7 +407,7 @@ def run_ours(args, world, rank, local):
                        "m": M, "n": N, "k": K, "moduli": S, "phi": PHI,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "no flush: inputs (2 GiB each) and planes are far larger than L2"},
-            "roofline": roofline, "phases": phases, "e2e": e2e,
+            "roofline": roofline, "phases": phases, "e2e": e2e, "scaling_variants": variants,
             "cpu_baseline": cpu_baseline_measure() if not args.no_cpu_baseline else None,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": clk, "context": context,
@@ -397,6 +431,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
+    ap.add_argument("--no-variants", action="store_true")
     args = ap.parse_args()
     world, rank, local = dist_env()
     if args.impl == "reference":

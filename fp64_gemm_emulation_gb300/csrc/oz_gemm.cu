@@ -7,9 +7,10 @@
 // accumulator in tensor memory adds integers exactly while |partial sum| <= 2^24.
 // The k loop is therefore cut into chunks of 1024 (1024 * 2^14 = 2^24).  Each chunk
 // starts from zero in one of two alternating TMEM accumulators; the epilogue warps read
-// it (tcgen05.ld), hand the accumulator straight back to the MMA, reduce the 32 values
-// of each load exactly mod m_t in FP32 and add them, mod m_t, to running residues held
-// in registers (two 16-bit lanes per register).  After the tile's last chunk the
+// it (tcgen05.ld), hand the accumulator straight back to the MMA, take each value to a
+// representative in (-m_t, m_t) with one FP32 quotient (exact) and add it plus m_t to
+// running sums held in registers (two 16-bit lanes per register, one integer add per two
+// values), which are reduced mod m_t only every 64 chunks and at the tile's end.  After the tile's last chunk the
 // residues go through shared memory to coalesced 16-byte stores of the uint8 plane.
 // This replaces the pages' block multiplication for k >= 2^17: the result is exact for
 // every k.  The same engine in exact mode (Scheme I) converts each chunk to INT32 and
@@ -97,6 +98,27 @@ __device__ __forceinline__ float exact_mod(float v, float m, float inv_m) {
   const float q = fmaf(v, inv_m, 12582912.0f) - 12582912.0f;
   const float r = fmaf(-q, m, v);
   return r < 0.0f ? r + m : r;
+}
+
+// v - m round(v/m) for an integer-valued float v (|v| < 2^25): exact, in (-m, m) (the
+// quotient of exact_mod without its fix-up).
+__device__ __forceinline__ float near_mod(float v, float m, float inv_m) {
+  const float q = fmaf(v, inv_m, 12582912.0f) - 12582912.0f;
+  return fmaf(-q, m, v);
+}
+
+// Chunks a 16-bit running lane can take between reductions: each adds less than 2m <= 512
+// to a lane that starts below m <= 256, and 256 + 64 * 511 < 2^16.
+constexpr int kLaneChunks = 64;
+
+// Reduces both 16-bit lanes of every register mod m (a lane < 2^16 is exact in FP32).
+__device__ __forceinline__ void reduce_lanes(uint32_t (&run)[64], float m, float inv_m) {
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const float lo = exact_mod(static_cast<float>(run[i] & 0xFFFFu), m, inv_m);
+    const float hi = exact_mod(static_cast<float>(run[i] >> 16), m, inv_m);
+    run[i] = __byte_perm(__float_as_uint(lo + 8388608.0f), __float_as_uint(hi + 8388608.0f), 0x5410);
+  }
 }
 
 // Rendezvous of the epilogue warps on an mbarrier (one arrival per warp), with the same
@@ -437,8 +459,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         const float mf = c.modf[uc.t], inv = c.invf[uc.t];
-        const uint32_t mm2 = static_cast<uint32_t>(mf) * 0x10001u;  // m in both 16-bit halves
-        // running residues of this thread's 128 columns, two per register (16-bit lanes)
+        const float bias = mf + 8388608.0f;  // r + m + 2^23: its low bits are the integer r + m
+        // Running sums of this thread's 128 columns, two per register (16-bit lanes).  Each
+        // chunk adds r + m with r = v - m round(v/m) in (-m, m), i.e. less than 2m <= 512 per
+        // lane; reducing the lanes mod m every kLaneChunks chunks keeps them below 2^16.
         uint32_t run[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) run[i] = 0;
@@ -463,15 +487,13 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float r0 = exact_mod(__uint_as_float(v[2 * i]), mf, inv);
-              const float r1 = exact_mod(__uint_as_float(v[2 * i + 1]), mf, inv);
-              // two residues as 16-bit lanes: low halves of 2^23 + r
-              const uint32_t p = __byte_perm(__float_as_uint(r0 + 8388608.0f), __float_as_uint(r1 + 8388608.0f),
-                                             0x5410);
-              const uint32_t s = __vadd2(run[cb * 16 + i], p);  // < 2m per lane
-              run[cb * 16 + i] = s - (__vcmpgeu2(s, mm2) & mm2);  // back into [0, m)
+              const float r0 = near_mod(__uint_as_float(v[2 * i]), mf, inv) + bias;
+              const float r1 = near_mod(__uint_as_float(v[2 * i + 1]), mf, inv) + bias;
+              run[cb * 16 + i] += __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x5410);
             }
           }
+          // keep the lanes below 2^16; after the last chunk every lane is in [0, m)
+          if ((ch + 1) % kLaneChunks == 0 || ch + 1 == nchunks) reduce_lanes(run, mf, inv);
         }
         if (!ok) break;
         // This K-block's residues join the tile's running result in the stash ([col][row]
