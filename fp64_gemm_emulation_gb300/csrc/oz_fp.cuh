@@ -21,4 +21,19 @@ __device__ __forceinline__ int ceil_log2_code(double x) {
   return (ex - 1023) + (f != 0 ? 1 : 0);
 }
 
+// floor(log2 |x|) from the IEEE-754 fields; OZ_EXP_EMPTY for 0, OZ_EXP_NONFINITE for Inf/NaN.
+__device__ __forceinline__ int floor_log2_code(double x) {
+  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;
+  if (b == 0) return OZ_EXP_EMPTY;
+  const int ex = static_cast<int>(b >> 52);
+  if (ex == 0x7FF) return OZ_EXP_NONFINITE;
+  if (ex == 0) return -1075 + (64 - __clzll(static_cast<long long>(b)));  // subnormal: f 2^-1074
+  return ex - 1023;
+}
+
+template <bool kFloor>
+__device__ __forceinline__ int log2_code(double x) {
+  return kFloor ? floor_log2_code(x) : ceil_log2_code(x);
+}
+
 }  // namespace oz

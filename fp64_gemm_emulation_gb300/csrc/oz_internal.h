@@ -44,15 +44,19 @@ constexpr int kMaxPairs = OZ_MAX_SLICES * (OZ_MAX_SLICES + 1) / 2;  // Scheme I 
 // pair; product p multiplies A plane a_plane[p] by B plane b_plane[p].
 //   residue mode (Scheme II): product t = modulus t, planes t and t, epilogue mod m_t;
 //   exact mode (Scheme I):    product p = slice pair (i, j), exact INT32 output.
+// The Scheme I accumulation reads the same structure: with grouped set, its batch t is the
+// sum of the pair products prod_first[t] .. prod_first[t+1]-1 (group-wise accumulation).
 struct GemmConsts {
   int s;              // number of products
   int kb_per_chunk;   // k-blocks of 64 whose FP32 sum stays exact
   int kb_per_block;   // k-blocks of 64 per scheduling K-block (a multiple of kb_per_chunk)
   uint32_t launch_id; // selects this launch's pacing counter
+  int grouped;        // accumulation only: the number of batches in prod_first (0: none)
   float modf[kMaxModuli];
   float invf[kMaxModuli];
   uint8_t a_plane[kMaxPairs];
   uint8_t b_plane[kMaxPairs];
+  uint8_t prod_first[kMaxPairs + 1];
 };
 
 // Host-side helpers (ozaki_host.cu).
@@ -63,6 +67,8 @@ int half_range_log2(int s);  // L = floor(log2(M/2 - 1)) for the first s moduli;
 // Kernel launchers; each returns a cudaError_t from the launch.
 cudaError_t launch_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                              int32_t* rowexp, int32_t* colexp, cudaStream_t stream);
+cudaError_t launch_floor_exponents(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                                   int32_t* rowexp, int32_t* colexp, cudaStream_t stream);
 cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,
                          const int32_t* exps, const SplitConsts& c, uint16_t* planes, int rows_padded,
                          int kp, cudaStream_t stream);

@@ -25,6 +25,8 @@ OZ_EXP_NONFINITE = np.int32(0x7FFFFFFF)
 PAD_M, PAD_N, PAD_K = 256, 256, 64
 OZ_NOALLOC_SCRATCH_BYTES = 64 << 20
 OZ_SCALE_UNIFORM, OZ_SCALE_FAST, OZ_SCALE_ACCU = 0, 1, 2
+OZ_OZAKI1_RN, OZ_OZAKI1_EF, OZ_OZAKI1_HYBRID = 0, 1, 2
+OZAKI1_VARIANTS = {"rn": OZ_OZAKI1_RN, "ef": OZ_OZAKI1_EF, "hybrid": OZ_OZAKI1_HYBRID}
 SCALINGS = {"uniform": OZ_SCALE_UNIFORM, "fast": OZ_SCALE_FAST, "accu": OZ_SCALE_ACCU}
 
 
@@ -68,6 +70,15 @@ def _load():
         "ozaki1_accumulate": (I, [I, I, I, I, P, P, P, P, I, P]),
         "ozaki1_dgemm_ws": (I, [I, I, I, P, I, P, I, P, I, I, P, S, P]),
         "ozaki1_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
+        "ozaki1_group_r": (I, [L, P]),
+        "ozaki1_num_batches": (I, [I, L, I, P]),
+        "ozaki1_split_scratch_bytes_ex": (S, [I, I, I, I]),
+        "ozaki1_workspace_bytes_ex": (S, [I, I, I, I, I]),
+        "ozaki1_split_ex": (I, [I, I, I, P, I, P, I, I, I, P, P, P, P, P, S, P]),
+        "ozaki1_slice_gemm_ex": (I, [I, I, I, I, I, P, P, P, P]),
+        "ozaki1_accumulate_ex": (I, [I, I, I, I, I, P, P, P, P, I, P]),
+        "ozaki1_dgemm_ex_ws": (I, [I, I, I, P, I, P, I, P, I, I, I, P, S, P]),
+        "ozaki1_dgemm_ex": (I, [I, I, I, P, I, P, I, P, I, I, I, P]),
         "ozaki_get_device_status": (I, []),
         "ozaki_status_string": (ctypes.c_char_p, [I]),
     }
@@ -408,6 +419,97 @@ def ozaki1_dgemm_ws(A, B, num_slices: int, workspace, C=None, stream=None):
                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
            "ozaki1_dgemm_ws")
     return C
+
+
+# ------------------------------------------------------------------ Scheme I variants
+def _variant(v) -> int:
+    return OZAKI1_VARIANTS[v] if isinstance(v, str) else int(v)
+
+
+def ozaki1_group_r(k_inner: int) -> int:
+    r = ctypes.c_int()
+    _check(_lib.ozaki1_group_r(k_inner, ctypes.byref(r)), "ozaki1_group_r")
+    return r.value
+
+
+def ozaki1_num_batches(num_slices: int, k_inner: int, variant="rn") -> int:
+    c = ctypes.c_int()
+    _check(_lib.ozaki1_num_batches(num_slices, k_inner, _variant(variant), ctypes.byref(c)), "ozaki1_num_batches")
+    return c.value
+
+
+def ozaki1_split_scratch_bytes_ex(m: int, n: int, k: int, variant="rn") -> int:
+    return int(_lib.ozaki1_split_scratch_bytes_ex(m, n, k, _variant(variant)))
+
+
+def ozaki1_workspace_bytes_ex(m: int, n: int, k: int, num_slices: int, variant="rn") -> int:
+    return int(_lib.ozaki1_workspace_bytes_ex(m, n, k, num_slices, _variant(variant)))
+
+
+def ozaki1_split_ex(A, B, num_slices: int, variant="rn", stream=None):
+    """Split of a variant: (A_planes, B_planes, A_exps, B_exps) as ozaki1_split."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    v = _variant(variant)
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    Ap = torch.empty((num_slices, mp, kp), dtype=torch.int16, device=A.device)
+    Bp = torch.empty((num_slices, np_, kp), dtype=torch.int16, device=A.device)
+    Ae = torch.empty((num_slices, m), dtype=torch.int32, device=A.device)
+    Be = torch.empty((num_slices, n), dtype=torch.int32, device=A.device)
+    nbytes = ozaki1_split_scratch_bytes_ex(m, n, k, v)
+    scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=A.device)
+    sp = (scratch.data_ptr() + 255) // 256 * 256
+    _check(_lib.ozaki1_split_ex(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_slices, v, _ptr(Ap), _ptr(Bp),
+                                _ptr(Ae), _ptr(Be), sp, nbytes, _stream(stream)), "ozaki1_split_ex")
+    return Ap, Bp, Ae, Be
+
+
+def ozaki1_slice_gemm_ex(m: int, n: int, k: int, num_slices: int, variant, A_planes, B_planes, stream=None):
+    """Exact INT32 pair products of a variant, in its order: [s(s+1)/2, Np, Mp]."""
+    import torch
+
+    v = _variant(variant)
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    P = torch.empty((num_slices * (num_slices + 1) // 2, np_, mp), dtype=torch.int32, device=A_planes.device)
+    _check(_lib.ozaki1_slice_gemm_ex(m, n, k, num_slices, v, _ptr(A_planes), _ptr(B_planes), _ptr(P),
+                                     _stream(stream)), "ozaki1_slice_gemm_ex")
+    return P
+
+
+def ozaki1_accumulate_ex(m: int, n: int, k: int, num_slices: int, variant, products, A_exps, B_exps, C=None,
+                         stream=None):
+    import torch
+
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=products.device).t()
+    _check(_lib.ozaki1_accumulate_ex(m, n, k, num_slices, _variant(variant), _ptr(products), _ptr(A_exps),
+                                     _ptr(B_exps), _ptr(C), _ld(C), _stream(stream)), "ozaki1_accumulate_ex")
+    return C
+
+
+def ozaki1_dgemm_ex(A, B, num_slices: int = 7, variant="rn", C=None, workspace=None, stream=None):
+    """C = A B by Scheme I in a variant ("rn", "ef", "hybrid"); with ``workspace`` the _ws form."""
+    import torch
+
+    m, k = A.shape
+    n = B.shape[1]
+    v = _variant(variant)
+    if C is None:
+        C = torch.empty((n, m), dtype=torch.float64, device=A.device).t()
+    if workspace is None:
+        rc = _lib.ozaki1_dgemm_ex(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_slices, v,
+                                  _stream(stream))
+    else:
+        rc = _lib.ozaki1_dgemm_ex_ws(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), _ptr(C), _ld(C), num_slices, v,
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "ozaki1_dgemm_ex")
+    return C
+
+
+def ozaki1_dgemm_ex_ws(A, B, num_slices: int, variant, workspace, C=None, stream=None):
+    return ozaki1_dgemm_ex(A, B, num_slices, variant, C=C, workspace=workspace, stream=stream)
 
 
 def ozaki_get_device_status() -> int:

@@ -24,6 +24,7 @@ def main():
     ap.add_argument("--scheme", type=int, choices=[1, 2], default=2)
     ap.add_argument("--slices", type=int, default=7)
     ap.add_argument("--scaling", choices=["uniform", "fast", "accu"], default="uniform")
+    ap.add_argument("--variant", choices=["rn", "ef", "hybrid"], default="rn", help="Scheme I split/accumulation")
     a = ap.parse_args()
     if a.scheme == 1:
         return run_scheme1(a)
@@ -81,36 +82,38 @@ def run_scheme1(a):
     from fp64_gemm_emulation_gb300.inputs import hpl_like
 
     m, n, k, s = a.m, a.n, a.k, a.slices
+    v = oz.OZAKI1_VARIANTS[a.variant]
     A, B = hpl_like(m, n, k, phi=a.phi, seed=0)
     dA = torch.from_numpy(A.T.copy()).cuda().t()
     dB = torch.from_numpy(B.T.copy()).cuda().t()
     dC = torch.empty((n, m), dtype=torch.float64, device="cuda").t()
     mp, np_, kp = oz.ozaki2_plane_dims(m, n, k)
     npairs = s * (s + 1) // 2
+    nbatch = oz.ozaki1_num_batches(s, k, v)
     Ap = torch.empty((s, mp, kp), dtype=torch.int16, device="cuda")
     Bp = torch.empty((s, np_, kp), dtype=torch.int16, device="cuda")
     Ae = torch.empty((s, m), dtype=torch.int32, device="cuda")
     Be = torch.empty((s, n), dtype=torch.int32, device="cuda")
     P = torch.empty((npairs, np_, mp), dtype=torch.int32, device="cuda")
-    nb = oz.ozaki1_split_scratch_bytes(m, n, k)
+    nb = oz.ozaki1_split_scratch_bytes_ex(m, n, k, v)
     scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
     lib, st = oz._lib, torch.cuda.current_stream().cuda_stream
     p = lambda t: t.data_ptr()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     for _ in range(a.reps):
         ev[0].record()
-        rc = lib.ozaki1_split(m, n, k, p(dA), m, p(dB), k, s, p(Ap), p(Bp), p(Ae), p(Be), p(scratch), nb, st)
+        rc = lib.ozaki1_split_ex(m, n, k, p(dA), m, p(dB), k, s, v, p(Ap), p(Bp), p(Ae), p(Be), p(scratch), nb, st)
         ev[1].record()
-        rc |= lib.ozaki1_slice_gemm(m, n, k, s, p(Ap), p(Bp), p(P), st)
+        rc |= lib.ozaki1_slice_gemm_ex(m, n, k, s, v, p(Ap), p(Bp), p(P), st)
         ev[2].record()
-        rc |= lib.ozaki1_accumulate(m, n, k, s, p(P), p(Ae), p(Be), p(dC), m, st)
+        rc |= lib.ozaki1_accumulate_ex(m, n, k, s, v, p(P), p(Ae), p(Be), p(dC), m, st)
         ev[3].record()
         if rc:
             raise SystemExit(f"ozaki1 call failed: {rc}")
     torch.cuda.synchronize()
     status = oz.ozaki_get_device_status()
     t = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
-    print(f"scheme I {m}x{n}x{k} s={s} ({npairs} products): split {t[0]:.3f} ms, slice_gemm {t[1]:.3f} ms, "
+    print(f"scheme I {a.variant} {m}x{n}x{k} s={s} ({npairs} products, {nbatch} FP64 terms): split {t[0]:.3f} ms, slice_gemm {t[1]:.3f} ms, "
           f"accumulate {t[2]:.3f} ms; gemm {npairs * 2.0 * m * n * k / (t[1] * 1e-3) / 1e12:.1f} TFLOP/s; "
           f"emulated {2.0 * m * n * k / (sum(t) * 1e-3) / 1e12:.1f} TFLOPS; status {status}")
     if status:

@@ -239,6 +239,58 @@ int ozaki1_dgemm_ws(int m, int n, int k, const double* A, int lda, const double*
                     cudaStream_t stream);
 int ozaki1_dgemm(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                  double* C, int ldc, int num_slices, cudaStream_t stream);
+/* ---------------------------------------------------------------- Scheme I variants */
+
+/* [Ozaki notes], "group-wise error-free accumulation" and "Hybrid":
+ *  OZ_OZAKI1_RN:     the RN split and one FP64 addition per slice product (the entry points
+ *                    above);
+ *  OZ_OZAKI1_EF:     the bitmask split (SplitInt): with e_i = floor(log2 max_j |a_ij|),
+ *                    slice p of a_ij is the p-th beta-bit field of |a_ij| below 2^(e_i + 1)
+ *                    (truncation), signed, scale 2^(e_i + 1 - p beta); A_exps[p][i] holds
+ *                    e_i + 1 - (p+1) beta (p 0-based), 0 for zero rows;
+ *  OZ_OZAKI1_HYBRID: the RN split with the fixed grid mu''_i = 2^(ceil(log2 max_j |a_ij|)
+ *                    + 1 - beta) lowered by 2^beta per slice (sigma = 0.75 2^(53 - beta p)
+ *                    mu''_i for 0-based p); A_exps[p][i] = log2 of that grid.
+ * EF and Hybrid accumulate group-wise: the pair products are ordered by group g = i + j
+ * (g = 2..s+1, i = 1..g-1 ascending) and products[t] is pair t in that order; the pairs
+ * of a group are summed exactly in INT32 in batches of r = max(1, 2^(31 - 2 beta -
+ * ceil(log2 k))) (ozaki1_group_r), and C = sum over the batches, in order, of the batch
+ * scaled by the power of two of its group, one FP64 round-to-nearest addition each, from +0.
+ * Hybrid supports row maxima in [2^(beta s - 1022), 2^960] (every grid a normal number);
+ * EF supports any finite input. */
+#define OZ_OZAKI1_RN 0
+#define OZ_OZAKI1_EF 1
+#define OZ_OZAKI1_HYBRID 2
+
+/* r for the inner dimension k_inner (host only; OZ_ERANGE as ozaki1_beta). */
+int ozaki1_group_r(long long k_inner, int* r_out);
+
+/* Terms of the FP64 accumulation for a variant: s(s+1)/2 pairs (RN) or the number of
+ * group batches (EF, Hybrid).  Every variant's slice GEMM writes s(s+1)/2 INT32 planes. */
+int ozaki1_num_batches(int num_slices, long long k_inner, int variant, int* count_out);
+
+/* Scratch of ozaki1_split_ex and workspace of ozaki1_dgemm_ex_ws for a variant. */
+size_t ozaki1_split_scratch_bytes_ex(int m, int n, int k, int variant);
+size_t ozaki1_workspace_bytes_ex(int m, int n, int k, int num_slices, int variant);
+
+/* The steps and the whole product for a variant (layouts as for the RN entry points;
+ * products holds s(s+1)/2 planes [pair][Np][Mp] of int32, pairs in the variant's order). */
+int ozaki1_split_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    int num_slices, int variant, uint16_t* A_planes, uint16_t* B_planes,
+                    int32_t* A_exps, int32_t* B_exps, void* scratch, size_t scratch_bytes,
+                    cudaStream_t stream);
+int ozaki1_slice_gemm_ex(int m, int n, int k, int num_slices, int variant,
+                         const uint16_t* A_planes, const uint16_t* B_planes, int32_t* products,
+                         cudaStream_t stream);
+int ozaki1_accumulate_ex(int m, int n, int k, int num_slices, int variant,
+                         const int32_t* products, const int32_t* A_exps, const int32_t* B_exps,
+                         double* C, int ldc, cudaStream_t stream);
+int ozaki1_dgemm_ex_ws(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                       double* C, int ldc, int num_slices, int variant, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+int ozaki1_dgemm_ex(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                    double* C, int ldc, int num_slices, int variant, cudaStream_t stream);
+
 
 /* ---------------------------------------------------------------- without allocation */
 

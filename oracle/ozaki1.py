@@ -215,7 +215,7 @@ def ozaki1_dgemm_variant(A: np.ndarray, B: np.ndarray, s: int, variant: str, bet
             acc = acc + exact_int_matmul(SA[i - 1], SBt[j - 1].T)   # exact INT products
         assert np.abs(acc).max(initial=0) < 2**31                     # the INT32 sum is exact
         x = XA[pairs[0][0] - 1][:, None] + XB[pairs[0][1] - 1][None, :]
-        for i, j in pairs:  # every pair of the group has the same scale
-            assert np.array_equal(XA[i - 1][:, None] + XB[j - 1][None, :], x) or not acc.any()
+        for i, j in pairs:  # every pair of the group has the same scale where the batch is nonzero
+            assert not ((XA[i - 1][:, None] + XB[j - 1][None, :] != x) & (acc != 0)).any()
         C = C + np.ldexp(acc.astype(np.float64), x)
     return C, SA, XA, SBt, XB, beta

@@ -175,3 +175,33 @@ def test_scaling_argument_errors(oz):
     # split / crt reject an unknown mode
     assert lib.ozaki2_split_ex(8, 8, 8, 1, 8, 1, 8, 14, 5, 1, 1, 1, 1, null) == oz.OZ_EINVAL
     assert lib.ozaki2_crt_ex(8, 8, 8, 14, 5, 1, 1, 1, 1, 8, null) == oz.OZ_EINVAL
+
+
+# ------------------------------------------------------------------ Scheme I variants
+@pytest.mark.parametrize("q", [1, 2, 255, 4096, 4097, 16384, 2**17, 2**17 + 1, 262144])
+def test_ozaki1_group_r_and_products_match_the_oracle(oz, q):
+    from oracle import ozaki1 as O1
+
+    beta = O1.beta_rn(q)
+    if beta < 1:
+        return
+    assert oz.ozaki1_group_r(q) == O1.group_r(q, beta)
+    for s in (1, 3, 7, 9, 20):
+        assert oz.ozaki1_num_batches(s, q, "rn") == s * (s + 1) // 2
+        want = len(O1.group_batches(s, O1.group_r(q, beta)))
+        assert oz.ozaki1_num_batches(s, q, "ef") == want
+        assert oz.ozaki1_num_batches(s, q, "hybrid") == want
+
+
+def test_ozaki1_variant_workspace_and_errors(oz):
+    lib, null = oz._lib, None
+    m, n, k = 300, 520, 2100
+    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn") == oz.ozaki1_workspace_bytes(m, n, k, 7)
+    # EF needs no residual arrays
+    assert oz.ozaki1_split_scratch_bytes_ex(m, n, k, "ef") < oz.ozaki1_split_scratch_bytes_ex(m, n, k, "rn")
+    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "ef") < oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn")
+    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "hybrid") == oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn")
+    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, 3) == 0
+    assert lib.ozaki1_dgemm_ex(8, 4, 4, 1, 8, 1, 4, 1, 8, 7, 3, null) == oz.OZ_EINVAL
+    assert lib.ozaki1_dgemm_ex_ws(8, 8, 8, 1, 8, 1, 8, 1, 8, 7, 1, 256, 16, null) == oz.OZ_ENOMEM
+    assert lib.ozaki1_num_batches(0, 16, 1, ctypes.byref(ctypes.c_int())) == oz.OZ_EINVAL
