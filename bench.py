@@ -147,6 +147,11 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def job_value(world: int, flops_per_step: float, steps: int, job_ms: float) -> float:
+    """Whole-job throughput in TFLOPS: the work of all ranks over the slowest rank's time."""
+    return world * flops_per_step * steps / (job_ms * 1e-3) / 1e12
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -298,7 +303,7 @@ def run_ours(args, world, rank, local):
     phase_ms /= args.steps
     job_ms = reduce_max(elapsed_ms, world, device)
     flops = 2.0 * M * N * K
-    value = world * flops * args.steps / (job_ms * 1e-3) / 1e12
+    value = job_value(world, flops, args.steps, job_ms)
 
     # ---- roofline of the dominant kernel (the residue GEMM), per launch
     gemm_ms = phase_ms[2]
