@@ -602,11 +602,13 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
     if ((rc = ozaki2_choose_k(num_moduli, k, &kA))) return rc;
   }
   // Two-dimensional block pipeline: row blocks of A x column blocks of B.  Copies in on one
-  // stream, the path on a second, copies out on a third, so block (i, j) computes while the
-  // next operand blocks arrive and finished blocks of C leave.
+  // stream (A_0, B_0, A_1, B_1, ...), the path on a second, copies out on a third; the blocks
+  // (i, j) are computed in the order their operands arrive (a square wavefront), so only the
+  // first two operand blocks and the last block's copy out are not hidden behind compute.
   const int s = num_moduli;
-  const Blocks mb = make_blocks(m, m >= 4096 ? 2 : 1);
-  const Blocks nbk = make_blocks(n, n >= 8192 ? 4 : (n >= 2048 ? 2 : 1));
+  auto block_count = [](int d) { return d >= 12288 ? 4 : (d >= 2048 ? 2 : 1); };
+  const Blocks mb = make_blocks(m, block_count(m));
+  const Blocks nbk = make_blocks(n, block_count(n));
   const int kp = static_cast<int>(roundup(k, kPadK));
   size_t off = 0;
   const size_t off_dA = off;
@@ -668,51 +670,77 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
   int32_t* colexp = reinterpret_cast<int32_t*>(ws + off_colexp);
   uint8_t* Cr = ws + off_Cr;
 
-  // copies in: A_0, B_0 .. B_last, A_1 .. A_last (the order the blocks are consumed)
+  // copies in, interleaved: A_0, B_0, A_1, B_1, ... (the order the wavefront consumes them)
   auto copy_A = [&](int i) {
     if (!rc && (cudaMemcpy2DAsync(dA + mb.start[i], sizeof(double) * m, A + mb.start[i], sizeof(double) * lda,
                                   sizeof(double) * mb.size[i], k, cudaMemcpyHostToDevice, sin) != cudaSuccess ||
                 cudaEventRecord(evA[i], sin) != cudaSuccess))
       rc = OZ_ECUDA;
   };
-  copy_A(0);
-  for (int j = 0; j < nbk.count && !rc; ++j) {
-    if (cudaMemcpy2DAsync(dB + static_cast<size_t>(nbk.start[j]) * k, sizeof(double) * k,
-                          B + static_cast<size_t>(nbk.start[j]) * ldb, sizeof(double) * ldb, sizeof(double) * k,
-                          nbk.size[j], cudaMemcpyHostToDevice, sin) != cudaSuccess ||
-        cudaEventRecord(evB[j], sin) != cudaSuccess)
+  auto copy_B = [&](int j) {
+    if (!rc && (cudaMemcpy2DAsync(dB + static_cast<size_t>(nbk.start[j]) * k, sizeof(double) * k,
+                                  B + static_cast<size_t>(nbk.start[j]) * ldb, sizeof(double) * ldb,
+                                  sizeof(double) * k, nbk.size[j], cudaMemcpyHostToDevice, sin) != cudaSuccess ||
+                cudaEventRecord(evB[j], sin) != cudaSuccess))
+      rc = OZ_ECUDA;
+  };
+  for (int q = 0; q < mb.count || q < nbk.count; ++q) {
+    if (q < mb.count) copy_A(q);
+    if (q < nbk.count) copy_B(q);
+  }
+
+  // block order: by the copy after which both operands are in (A_i is copy 2i, B_j copy
+  // 2j + 1 while both lists last), then row, then column
+  int order[Blocks::kMax * Blocks::kMax];
+  int nblocks = 0;
+  auto arrival = [&](int i, int j) {
+    const int ai = i < nbk.count ? 2 * i : nbk.count + i;
+    const int bj = j < mb.count ? 2 * j + 1 : mb.count + j;
+    return ai > bj ? ai : bj;
+  };
+  for (int i = 0; i < mb.count; ++i)
+    for (int j = 0; j < nbk.count; ++j) order[nblocks++] = i * nbk.count + j;
+  for (int a = 1; a < nblocks; ++a)  // insertion sort, stable: (arrival, i, j)
+    for (int b = a; b > 0 && arrival(order[b] / nbk.count, order[b] % nbk.count) <
+                                  arrival(order[b - 1] / nbk.count, order[b - 1] % nbk.count);
+         --b) {
+      const int t = order[b];
+      order[b] = order[b - 1];
+      order[b - 1] = t;
+    }
+
+  // the path, block by block; each operand block is scaled and split when first needed
+  bool splitA[Blocks::kMax] = {}, splitB[Blocks::kMax] = {};
+  for (int b = 0; b < nblocks && !rc; ++b) {
+    const int i = order[b] / nbk.count, j = order[b] % nbk.count;
+    const int i0 = mb.start[i], mi = mb.size[i];
+    const int j0 = nbk.start[j], nj = nbk.size[j];
+    uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + off_Ap[i]);
+    uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + off_Bp[j]);
+    const double* dBj = dB + static_cast<size_t>(j0) * k;
+    if (!splitA[i]) {
+      if (cudaStreamWaitEvent(scomp, evA[i], 0) != cudaSuccess) rc = OZ_ECUDA;
+      if (!rc) rc = ozaki2_exponents(mi, 0, k, dA + i0, m, nullptr, 1, rowexp + i0, nullptr, scomp);
+      if (!rc) rc = ozaki2_split(mi, 0, k, dA + i0, m, nullptr, 1, s, rowexp + i0, nullptr, Ap, nullptr, scomp);
+      splitA[i] = true;
+    }
+    if (!splitB[j]) {
+      if (!rc && cudaStreamWaitEvent(scomp, evB[j], 0) != cudaSuccess) rc = OZ_ECUDA;
+      if (!rc) rc = ozaki2_exponents(0, nj, k, nullptr, 1, dBj, k, nullptr, colexp + j0, scomp);
+      if (!rc) rc = ozaki2_split(0, nj, k, nullptr, 1, dBj, k, s, nullptr, colexp + j0, nullptr, Bp, scomp);
+      splitB[j] = true;
+    }
+    if (!rc) rc = ozaki2_residue_gemm(mi, nj, k, s, Ap, Bp, Cr, scomp);
+    double* dCij = dC + i0 + static_cast<size_t>(j0) * m;
+    if (!rc) rc = ozaki2_crt(mi, nj, k, s, Cr, rowexp + i0, colexp + j0, dCij, m, scomp);
+    cudaEvent_t e = evC[i * nbk.count + j];
+    if (!rc && (cudaEventRecord(e, scomp) != cudaSuccess || cudaStreamWaitEvent(sout, e, 0) != cudaSuccess ||
+                cudaMemcpy2DAsync(C + i0 + static_cast<size_t>(j0) * ldc, sizeof(double) * ldc, dCij,
+                                  sizeof(double) * m, sizeof(double) * mi, nj, cudaMemcpyDeviceToHost,
+                                  sout) != cudaSuccess))
       rc = OZ_ECUDA;
   }
-  for (int i = 1; i < mb.count; ++i) copy_A(i);
-
-  // the path, block by block
-  for (int i = 0; i < mb.count && !rc; ++i) {
-    const int i0 = mb.start[i], mi = mb.size[i];
-    uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + off_Ap[i]);
-    if (cudaStreamWaitEvent(scomp, evA[i], 0) != cudaSuccess) rc = OZ_ECUDA;
-    if (!rc) rc = ozaki2_exponents(mi, 0, k, dA + i0, m, nullptr, 1, rowexp + i0, nullptr, scomp);
-    if (!rc) rc = ozaki2_split(mi, 0, k, dA + i0, m, nullptr, 1, s, rowexp + i0, nullptr, Ap, nullptr, scomp);
-    for (int j = 0; j < nbk.count && !rc; ++j) {
-      const int j0 = nbk.start[j], nj = nbk.size[j];
-      uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + off_Bp[j]);
-      const double* dBj = dB + static_cast<size_t>(j0) * k;
-      if (i == 0) {
-        if (cudaStreamWaitEvent(scomp, evB[j], 0) != cudaSuccess) rc = OZ_ECUDA;
-        if (!rc) rc = ozaki2_exponents(0, nj, k, nullptr, 1, dBj, k, nullptr, colexp + j0, scomp);
-        if (!rc) rc = ozaki2_split(0, nj, k, nullptr, 1, dBj, k, s, nullptr, colexp + j0, nullptr, Bp, scomp);
-      }
-      if (!rc) rc = ozaki2_residue_gemm(mi, nj, k, s, Ap, Bp, Cr, scomp);
-      double* dCij = dC + i0 + static_cast<size_t>(j0) * m;
-      if (!rc) rc = ozaki2_crt(mi, nj, k, s, Cr, rowexp + i0, colexp + j0, dCij, m, scomp);
-      cudaEvent_t e = evC[i * nbk.count + j];
-      if (!rc && (cudaEventRecord(e, scomp) != cudaSuccess || cudaStreamWaitEvent(sout, e, 0) != cudaSuccess ||
-                  cudaMemcpy2DAsync(C + i0 + static_cast<size_t>(j0) * ldc, sizeof(double) * ldc, dCij,
-                                    sizeof(double) * m, sizeof(double) * mi, nj, cudaMemcpyDeviceToHost,
-                                    sout) != cudaSuccess))
-        rc = OZ_ECUDA;
-      (void)kp;
-    }
-  }
+  (void)kp;
   // release the workspace after the copies out, then wait for everything
   cudaEvent_t done = nullptr;
   if (ws) {

@@ -234,3 +234,15 @@ def test_host_pipeline_blocks_match_device_path(oz):
     rows, cols = [0, m - 1, 4095, 4096, 17], [n - 1, 0, 2047, 2048, 1000]
     want = O.direct_entries(A, B, 14, rows, cols)
     assert np.array_equal(bits(Ch[rows, cols]), bits(want))
+
+
+def test_host_pipeline_four_by_two_blocks(oz):
+    # m >= 12288: four row blocks (ragged last), n = 2100: two column blocks; the blocks are
+    # computed in the order their operands arrive (A_0, B_0, A_1, B_1, A_2, A_3)
+    m, n, k = 12300, 2100, 300
+    A, B = hpl_like(m, n, k, phi=0.5, seed=18)
+    Ch = np.empty((m, n), order="F")
+    rc = oz._lib.ozaki2_dgemm_host(m, n, k, A.ctypes.data, m, B.ctypes.data, k, Ch.ctypes.data, m, 14)
+    assert rc == 0
+    ref = host(oz.ozaki2_dgemm(dev(A), dev(B), 14))
+    assert np.array_equal(bits(Ch), bits(ref))
