@@ -36,6 +36,15 @@ PHI = 0.5
 SEED = 0
 PAGES_GH200_TFLOPS = 80.2  # the pages' Scheme II figure at 16384^3, s=14 (GH200): context
 KERNELS_PER_STEP = 6       # rowexp, colexp, split(A), split(B), residue GEMM, CRT
+# Figures the pages quote at 16384^3, each with its hardware: context only, not targets.
+PAGES_FIGURES = {
+    "GH200, Ozaki Scheme II, s=14": 80.2,
+    "B200, NVIDIA's emulated-FP64 peak specification (tensor-core emulation)": 150.0,
+    "RTX PRO 6000 Blackwell, OzII-FP4 (compute phase)": 17.31,
+    "RTX PRO 6000 Blackwell, GEMMul8-INT8 (compute phase)": 40.94,
+    "RTX PRO 6000 Blackwell, cuBLAS FP64": 1.85,
+    "unit": "TFLOPS",
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -419,6 +428,7 @@ def run_ours(args, world, rank, local):
             "tensor_path": "residues in bf16 on tcgen05 CTA pairs, exact FP32 accumulation in TMEM over "
                            "chunks of 1024 k, each chunk reduced mod m_t into register residues",
             "vs_baseline_ref": "pages' GH200 Scheme II figure, 80.2 TFLOPS (other hardware)",
+            "pages_figures": PAGES_FIGURES,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
