@@ -25,6 +25,7 @@ def main():
     ap.add_argument("--slices", type=int, default=7)
     ap.add_argument("--scaling", choices=["uniform", "fast", "accu"], default="uniform")
     ap.add_argument("--variant", choices=["rn", "ef", "hybrid"], default="rn", help="Scheme I split/accumulation")
+    ap.add_argument("--graph", action="store_true", help="also time the whole call captured in a CUDA graph")
     a = ap.parse_args()
     if a.scheme == 1:
         return run_scheme1(a)
@@ -71,7 +72,35 @@ def main():
           + f"; gemm {s * 2.0 * m * n * k / (t[2] * 1e-3) / 1e12:.1f} TFLOP/s; status {status}")
     if status:
         raise SystemExit(1)
+    if a.graph:
+        time_graph(oz, dA, dB, s, a.scaling, m, n, k)
     return np.float64(sum(t))
+
+
+def time_graph(oz, dA, dB, s, scaling, m, n, k, reps=50):
+    """Mean time of the whole Scheme II call per launch: eager vs replayed from a CUDA graph."""
+    import torch
+
+    C = torch.empty((n, m), dtype=torch.float64, device="cuda").t()
+    ws = torch.empty(oz.ozaki2_workspace_bytes_ex(m, n, k, s, scaling), dtype=torch.uint8, device="cuda")
+    oz.ozaki2_dgemm_ex_ws(dA, dB, s, scaling, ws, C=C)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        oz.ozaki2_dgemm_ex_ws(dA, dB, s, scaling, ws, C=C)
+    out = {}
+    for name, fn in (("eager", lambda: oz.ozaki2_dgemm_ex_ws(dA, dB, s, scaling, ws, C=C)), ("graph", g.replay)):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / reps
+    print(f"{m}x{n}x{k} s={s} {scaling}: whole call eager {out['eager'] * 1e3:.1f} us, "
+          f"CUDA graph {out['graph'] * 1e3:.1f} us per call ({2.0 * m * n * k / (out['graph'] * 1e-3) / 1e12:.2f} TFLOPS)")
 
 
 def run_scheme1(a):
