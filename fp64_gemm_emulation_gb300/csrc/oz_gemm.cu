@@ -431,23 +431,26 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
-#pragma unroll 1
-          for (int cb = 0; cb < 128; cb += 64) {
-            uint32_t v[32], w[32];
-            tmem_ld32(taddr + cb, v);
-            tmem_ld32(taddr + cb + 32, w);
-            tmem_ld_wait();
-            int32_t* o = base + static_cast<long long>(cb) * mp;
+          // the whole chunk into registers first, so the accumulator goes back to the MMA
+          // before the (slower) INT32 updates of the output
+          uint32_t v[4][32];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-              int32_t x = __float2int_rn(__uint_as_float(i < 32 ? v[i] : w[i - 32]));  // exact integer
-              if (kblk > 0 || ch > 0) x += o[static_cast<long long>(i) * mp];
-              o[static_cast<long long>(i) * mp] = x;
-            }
-          }
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32(taddr + cb * 32, v[cb]);
+          tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
+          const bool first = (kblk == 0 && ch == 0);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) {
+            int32_t* o = base + static_cast<long long>(cb * 32) * mp;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              int32_t x = __float2int_rn(__uint_as_float(v[cb][i]));  // exact integer
+              if (!first) x += o[static_cast<long long>(i) * mp];
+              o[static_cast<long long>(i) * mp] = x;
+            }
+          }
         }
       }
     } else {
