@@ -93,6 +93,22 @@ __device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
 
+// Shifted path (0 < p <= kShiftMax for some element, e.g. k_A > 53): a' = u 2^p < 2^63 as
+// four 16-bit limbs, y = x3 c48 + x2 c32 + x1 c16 + x0 with |y| < 2^26, then the same single
+// Barrett step as the fast path: BIG = m 2^22 exceeds |y| when every modulus is above 16
+// (SplitConsts::shift_ok), and ys < 2^31 <= 2^39 / m keeps the quotient exact.
+constexpr uint32_t kShiftMax = 10;
+
+__device__ __forceinline__ float residue_shifted(int sx0, int sx1, int sx2, int sx3, uint32_t negf, uint32_t m,
+                                                 uint32_t c16, uint32_t c32, uint32_t c48, uint32_t magic,
+                                                 uint32_t big, uint32_t halfm, uint32_t fbase) {
+  const uint32_t y = static_cast<uint32_t>(sx3 * static_cast<int>(c48) + sx2 * static_cast<int>(c32) +
+                                           sx1 * static_cast<int>(c16) + sx0);
+  const uint32_t ys = negf * big + y + halfm;
+  const uint32_t q = __umulhi(ys, magic) >> 7;
+  return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
+}
+
 // Residues of the 8 packed values of one thread modulo every modulus, written as 8 bf16
 // (16 bytes) per plane at dst + t * plane_elems.  Every lane of the warp must call it
 // (the p == 0 test is warp-uniform); lanes with dst == nullptr compute but do not store.
@@ -110,10 +126,45 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
     pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
     ng[x] = (v[x] >> 63) != 0;
   }
-  bool any_p = false;
+  bool any_p = false, big_p = false;
 #pragma unroll
-  for (int x = 0; x < 8; ++x) any_p |= (pp[x] != 0);
-  if (!__any_sync(0xFFFFFFFFu, any_p)) {
+  for (int x = 0; x < 8; ++x) {
+    any_p |= (pp[x] != 0);
+    big_p |= (pp[x] > kShiftMax);
+  }
+  const bool warp_any_p = __any_sync(0xFFFFFFFFu, any_p);
+  const bool warp_big_p = __any_sync(0xFFFFFFFFu, big_p);
+  if (warp_any_p && !warp_big_p && c.shift_ok) {
+    // every a' of the warp is u 2^p with p <= kShiftMax: four signed 16-bit limbs of u 2^p
+    int sx0[8], sx1[8], sx2[8], sx3[8];
+    uint32_t nf[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint64_t a = (v[x] & ((1ull << 53) - 1)) << pp[x];  // < 2^63
+      const int sg = ng[x] ? -1 : 1;
+      sx0[x] = sg * static_cast<int>(static_cast<uint32_t>(a) & 0xFFFFu);
+      sx1[x] = sg * static_cast<int>(static_cast<uint32_t>(a) >> 16);
+      sx2[x] = sg * static_cast<int>(static_cast<uint32_t>(a >> 32) & 0xFFFFu);
+      sx3[x] = sg * static_cast<int>(static_cast<uint32_t>(a >> 48));
+      nf[x] = ng[x] ? 1u : 0u;
+    }
+#pragma unroll 1
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], c48 = c.c48[t],
+                     mg = c.magic[t];
+      const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
+      uint32_t w[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float lo = residue_shifted(sx0[2 * x], sx1[2 * x], sx2[2 * x], sx3[2 * x], nf[2 * x], m, c16, c32,
+                                         c48, mg, big, halfm, fbase);
+        const float hi = residue_shifted(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], sx3[2 * x + 1],
+                                         nf[2 * x + 1], m, c16, c32, c48, mg, big, halfm, fbase);
+        w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
+      }
+      if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else if (!warp_any_p) {
     // common case: every a' of the warp is u itself (no power-of-two factor)
     int sx0[8], sx1[8], sx2[8];
     uint32_t nf[8];

@@ -145,11 +145,14 @@ int fill_split_consts(int s, long long k_inner, SplitConsts* out) {
   std::memset(out, 0, sizeof(*out));
   out->s = s;
   out->kA = k;
+  out->shift_ok = 1;
   for (int t = 0; t < s; ++t) {
     const uint32_t m = static_cast<uint32_t>(p.mod[t]);
+    if ((static_cast<uint64_t>(m) << 22) <= (1ull << 26)) out->shift_ok = 0;
     out->mod[t] = p.mod[t];
     out->c16[t] = (1u << 16) % m;
     out->c32[t] = static_cast<uint32_t>((1ull << 32) % m);
+    out->c48[t] = static_cast<uint32_t>((1ull << 48) % m);
     out->magic[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
   }
   return OZ_OK;
