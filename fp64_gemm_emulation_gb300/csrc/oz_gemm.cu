@@ -191,21 +191,34 @@ struct PairSchedule {
 constexpr int kModeResidue = 0;  // Scheme II: C''_t = (A'_t B'_t) mod m_t, uint8 output
 constexpr int kModeExact = 1;    // Scheme I: exact INT32 slice products
 constexpr int kModeMax = 2;      // OS II-accu: row and column maxima of one exact product
+constexpr int kModeExactAcc = 3; // Scheme I products of several exact chunks: INT32 sums in shared memory
+
+// Shared-memory layout per mode.  The running-sum mode trades three of the six stages for a
+// 128 KB INT32 tile (this CTA's 128 rows x 256 columns), so each product's chunks are summed
+// on chip and the output is written once.
+template <int MODE>
+struct ModeLayout {
+  static constexpr int STAGES = (MODE == kModeExactAcc) ? 3 : gemm::STAGES;
+  static constexpr uint32_t STASH = (MODE == kModeExactAcc) ? gemm::HALF_M * gemm::BN * 4 : gemm::STASH_BYTES;
+  static constexpr size_t SMEM = 1024 /*align slack*/ + STAGES * gemm::STAGE_BYTES + STASH + 256 /*barriers*/;
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
 
 template <int MODE>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmConsts c, void* __restrict__ out_ptr, int mp, int np, int nkb) {
   using namespace gemm;
+  constexpr int kStages = ModeLayout<MODE>::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE;
-  uint8_t* stash = smem + STAGES * STAGE_BYTES;  // [128 cols][128 rows]... see epilogue
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stash + STASH_BYTES);
-  uint64_t* full = bars;                  // [STAGES]  TMA (both CTAs) -> MMA   (used in the leader)
-  uint64_t* empty = bars + STAGES;        // [STAGES]  MMA -> TMA               (both CTAs)
-  uint64_t* accfull = bars + 2 * STAGES;  // [2]       MMA -> epilogue          (both CTAs)
+  uint8_t* sB = smem + kStages * A_STAGE;
+  uint8_t* stash = smem + kStages * STAGE_BYTES;  // [128 cols][128 rows]... see epilogue
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stash + ModeLayout<MODE>::STASH);
+  uint64_t* full = bars;                  // [kStages]  TMA (both CTAs) -> MMA   (used in the leader)
+  uint64_t* empty = bars + kStages;        // [kStages]  MMA -> TMA               (both CTAs)
+  uint64_t* accfull = bars + 2 * kStages;  // [2]       MMA -> epilogue          (both CTAs)
   uint64_t* accempty = accfull + 2;       // [2]       epilogues (both) -> MMA  (used in the leader)
   uint64_t* drain = accempty + 2;         // [1]       all MMAs of the pair done (both CTAs)
   uint64_t* epibar = drain + 1;           // [1]       epilogue warps rendezvous (per CTA)
@@ -222,7 +235,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   const PairSchedule sched(units, nkb, kbb);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 2);  // one arrival (with its bytes) from each CTA's producer
       mbar_init(&empty[i], 1);
     }
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           tma_load_3d_pair(sA + stage * A_STAGE, &tmA, full_leader, kb * BK, rowA, pa);
           tma_load_3d_pair(sB + stage * B_STAGE, &tmB, full_leader, kb * BK, rowB, pb);
           ++issued;
-          if (++stage == STAGES) {
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
@@ -299,9 +312,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       // consumed them on the normal path.  The copies complete on the leader's barriers,
       // which the leader's MMA thread drains (below); here wait for this CTA's stages to
       // be released by the MMAs that read them.
-      for (int i = 0; i < STAGES && i < issued; ++i) {
+      for (int i = 0; i < kStages && i < issued; ++i) {
         if (--stage < 0) {
-          stage = STAGES - 1;
+          stage = kStages - 1;
           phase ^= 1;
         }
         if (!mbar_wait(&empty[stage], phase)) record_timeout(abort_flag);
@@ -347,7 +360,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
               umma_bf16_pair(d_tmem, ad, bd, IDESC, accumulate);
             }
             umma_commit_pair(&empty[stage], 0x3);  // frees the stage in both CTAs
-            if (++stage == STAGES) {
+            if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
             }
@@ -411,6 +424,49 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           atomicMax(gamma + col0 + cb * 32 + lane, mine);
         }
         atomicMax(rho + uc.tm * BM + row_off + row, rmax);
+      }
+    } else if (MODE == kModeExactAcc) {
+      // This thread's slice of the INT32 tile: its row, columns half*128 .. +127, laid out
+      // [column][row] so a warp's 32 rows are 32 consecutive words.  Owned by this thread
+      // alone: no barrier.  Units cover the whole k range (one K-block).
+      int32_t* outp = static_cast<int32_t*>(out_ptr);
+      int32_t* mine = reinterpret_cast<int32_t*>(stash) + (half * 128) * HALF_M + row;
+      for (int idx = 0; idx < sched.count() && ok; ++idx) {
+        int u, kblk;
+        sched.at(idx, u, kblk);
+        const int kb_begin = kblk * kbb, kb_end = min(nkb, kb_begin + kbb);
+        const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
+        const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        for (int ch = 0; ch < nchunks; ++ch, ++g) {
+          const uint32_t acc = g & 1;
+          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+            ok = false;
+            if (lane == 0) record_timeout(abort_flag);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
+          uint32_t v[4][32];
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) tmem_ld32(taddr + cb * 32, v[cb]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int32_t x = __float2int_rn(__uint_as_float(v[cb][i]));  // exact integer
+              int32_t* p = mine + (cb * 32 + i) * HALF_M;
+              *p = (ch == 0) ? x : *p + x;
+            }
+        }
+        if (!ok) break;
+        int32_t* base =
+            outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row_off + row;
+#pragma unroll 8
+        for (int c2 = 0; c2 < 128; ++c2) base[static_cast<long long>(c2) * mp] = mine[c2 * HALF_M];
       }
     } else if (MODE == kModeExact) {
       int32_t* outp = static_cast<int32_t*>(out_ptr);
@@ -597,6 +653,12 @@ static bool make_plane_map(CUtensorMap* map, const void* base, int s, int rows, 
   return r == CUDA_SUCCESS;
 }
 
+// Exact chunks per product from which the slice GEMM keeps its running sums in shared memory
+// (three stages instead of six) rather than folding every chunk into the output through L2.
+// Measured at 8192^3 (Scheme I, 36 products): two chunks take 24.5 ms through L2 and 28.7 ms
+// on chip; every further chunk adds about 3.6 ms through L2, so on chip wins from four.
+constexpr int kAccChunks = 4;
+
 static uint32_t next_launch_id() {
   static uint32_t id = 0;
   return __atomic_add_fetch(&id, 1u, __ATOMIC_RELAXED);
@@ -613,7 +675,7 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   if (!make_plane_map(&tmA, A_planes, a_planes, mp, kp, HALF_M)) return OZ_ECUDA;
   if (!make_plane_map(&tmB, B_planes, b_planes, np, kp, HALF_N)) return OZ_ECUDA;
   if (cudaFuncSetAttribute(residue_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(SMEM_BYTES)) != cudaSuccess)
+                           static_cast<int>(ModeLayout<MODE>::SMEM)) != cudaSuccess)
     return OZ_ECUDA;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ_ECUDA;
@@ -623,7 +685,7 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = ModeLayout<MODE>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -656,6 +718,10 @@ int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint1
 
 int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,
                       const uint16_t* A_planes, const uint16_t* B_planes, int32_t* out, cudaStream_t stream) {
+  const int nkb = kp / gemm::BK;
+  const int chunks = c.kb_per_chunk > 0 ? (nkb + c.kb_per_chunk - 1) / c.kb_per_chunk : 1;
+  if (chunks >= kAccChunks && c.kb_per_block >= nkb)
+    return launch_gemm<kModeExactAcc>(mp, np, kp, a_planes, b_planes, c, A_planes, B_planes, out, stream);
   return launch_gemm<kModeExact>(mp, np, kp, a_planes, b_planes, c, A_planes, B_planes, out, stream);
 }
 
