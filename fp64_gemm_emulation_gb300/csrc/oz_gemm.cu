@@ -193,13 +193,14 @@ constexpr int kModeExact = 1;    // Scheme I: exact INT32 slice products
 constexpr int kModeMax = 2;      // OS II-accu: row and column maxima of one exact product
 constexpr int kModeExactAcc = 3; // Scheme I products of several exact chunks: INT32 sums in shared memory
 
-// Shared-memory layout per mode.  The running-sum mode trades three of the six stages for a
-// 128 KB INT32 tile (this CTA's 128 rows x 256 columns), so each product's chunks are summed
-// on chip and the output is written once.
+// Shared-memory layout per mode.  The running-sum mode keeps half of each thread's INT32
+// running sums in registers and half in a 64 KB shared-memory tile (this CTA's 128 rows x
+// 128 of its 256 columns), which costs one of the six stages; each product's chunks are
+// summed on chip and the output is written once.
 template <int MODE>
 struct ModeLayout {
-  static constexpr int STAGES = (MODE == kModeExactAcc) ? 3 : gemm::STAGES;
-  static constexpr uint32_t STASH = (MODE == kModeExactAcc) ? gemm::HALF_M * gemm::BN * 4 : gemm::STASH_BYTES;
+  static constexpr int STAGES = (MODE == kModeExactAcc) ? 5 : gemm::STAGES;
+  static constexpr uint32_t STASH = (MODE == kModeExactAcc) ? gemm::HALF_M * (gemm::BN / 2) * 4 : gemm::STASH_BYTES;
   static constexpr size_t SMEM = 1024 /*align slack*/ + STAGES * gemm::STAGE_BYTES + STASH + 256 /*barriers*/;
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -426,17 +427,19 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         atomicMax(rho + uc.tm * BM + row_off + row, rmax);
       }
     } else if (MODE == kModeExactAcc) {
-      // This thread's slice of the INT32 tile: its row, columns half*128 .. +127, laid out
-      // [column][row] so a warp's 32 rows are 32 consecutive words.  Owned by this thread
-      // alone: no barrier.  Units cover the whole k range (one K-block).
+      // This thread's 128 columns (its row, columns half*128 .. +127): the first 64 running
+      // sums live in registers, the other 64 in the shared tile, laid out [column][row] so a
+      // warp's 32 rows are 32 consecutive words.  Owned by this thread alone: no barrier.
+      // Units cover the whole k range (one K-block).
       int32_t* outp = static_cast<int32_t*>(out_ptr);
-      int32_t* mine = reinterpret_cast<int32_t*>(stash) + (half * 128) * HALF_M + row;
+      int32_t* mine = reinterpret_cast<int32_t*>(stash) + (half * 64) * HALF_M + row;
       for (int idx = 0; idx < sched.count() && ok; ++idx) {
         int u, kblk;
         sched.at(idx, u, kblk);
         const int kb_begin = kblk * kbb, kb_end = min(nkb, kb_begin + kbb);
         const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
+        int32_t run[64];
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
           if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
@@ -446,27 +449,35 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           }
           tc_fence_after();
           const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN + half * 128;
-          uint32_t v[4][32];
+          uint32_t v[2][32];
+          tmem_ld32(taddr, v[0]);
+          tmem_ld32(taddr + 32, v[1]);
+          tmem_ld_wait();
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb) tmem_ld32(taddr + cb * 32, v[cb]);
+          for (int c2 = 0; c2 < 64; ++c2) {
+            const int32_t x = __float2int_rn(__uint_as_float(v[c2 >> 5][c2 & 31]));  // exact integer
+            run[c2] = (ch == 0) ? x : run[c2] + x;
+          }
+          tmem_ld32(taddr + 64, v[0]);
+          tmem_ld32(taddr + 96, v[1]);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&accempty[acc]), 0));
 #pragma unroll
-          for (int cb = 0; cb < 4; ++cb)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int32_t x = __float2int_rn(__uint_as_float(v[cb][i]));  // exact integer
-              int32_t* p = mine + (cb * 32 + i) * HALF_M;
-              *p = (ch == 0) ? x : *p + x;
-            }
+          for (int c2 = 0; c2 < 64; ++c2) {
+            const int32_t x = __float2int_rn(__uint_as_float(v[c2 >> 5][c2 & 31]));
+            int32_t* p = mine + c2 * HALF_M;
+            *p = (ch == 0) ? x : *p + x;
+          }
         }
         if (!ok) break;
         int32_t* base =
             outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row_off + row;
+#pragma unroll
+        for (int c2 = 0; c2 < 64; ++c2) base[static_cast<long long>(c2) * mp] = run[c2];
 #pragma unroll 8
-        for (int c2 = 0; c2 < 128; ++c2) base[static_cast<long long>(c2) * mp] = mine[c2 * HALF_M];
+        for (int c2 = 0; c2 < 64; ++c2) base[static_cast<long long>(64 + c2) * mp] = mine[c2 * HALF_M];
       }
     } else if (MODE == kModeExact) {
       int32_t* outp = static_cast<int32_t*>(out_ptr);
@@ -653,11 +664,9 @@ static bool make_plane_map(CUtensorMap* map, const void* base, int s, int rows, 
   return r == CUDA_SUCCESS;
 }
 
-// Exact chunks per product from which the slice GEMM keeps its running sums in shared memory
-// (three stages instead of six) rather than folding every chunk into the output through L2.
-// Measured at 8192^3 (Scheme I, 36 products): two chunks take 24.5 ms through L2 and 28.7 ms
-// on chip; every further chunk adds about 3.6 ms through L2, so on chip wins from four.
-constexpr int kAccChunks = 4;
+// Exact chunks per product from which the slice GEMM keeps its running sums on chip (five
+// stages instead of six) rather than folding every chunk into the output through L2.
+constexpr int kAccChunks = 2;
 
 static uint32_t next_launch_id() {
   static uint32_t id = 0;
