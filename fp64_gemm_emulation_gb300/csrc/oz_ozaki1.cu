@@ -206,6 +206,117 @@ __global__ void __launch_bounds__(kThreads) bitmask_split_kernel(int rows, int K
   }
 }
 
+// Hybrid split in one pass ([Ozaki notes], Hybrid split): the grids mu''_i 2^(-beta (p-1))
+// are fixed by the input's row maximum (E = ceil(log2 max |x|), grid exponent E + 1 - beta p),
+// so every slice of an element follows from the element alone.  fl(r + sigma) - sigma with
+// sigma = 0.75 2^53 grid is round-half-to-even of r / grid, so it is done here exactly on the
+// integers: x = M 2^e2 (|M| < 2^53); slice p is q = RNE(M / 2^(ex - e2)) and M -= q 2^(ex - e2),
+// the same slices and residuals the double operations produce (every grid a normal number).
+template <bool kRowsContiguous>
+__global__ void __launch_bounds__(kThreads) hybrid_split_kernel(int rows, int K, const double* __restrict__ X,
+                                                                long long rs, long long ks,
+                                                                const int32_t* __restrict__ E, int ns, int beta,
+                                                                uint16_t* __restrict__ planes, int rows_padded,
+                                                                int kp, int32_t* __restrict__ exps) {
+  __shared__ uint64_t tile[kTile][kTile + 1];  // [kk][r] bits of x
+  const int tid = threadIdx.x;
+  const int k0 = blockIdx.x * kTile;
+  const int r0 = blockIdx.y * kTile;
+#pragma unroll 4
+  for (int it = 0; it < (kTile * kTile) / kThreads; ++it) {
+    int r, kk;
+    if (kRowsContiguous) {
+      r = tid & 63;
+      kk = (tid >> 6) + 4 * it;
+    } else {
+      kk = tid & 63;
+      r = (tid >> 6) + 4 * it;
+    }
+    const int gr = r0 + r, gk = k0 + kk;
+    tile[kk][r] = (gr < rows && gk < K) ? static_cast<uint64_t>(__double_as_longlong(X[gr * rs + gk * ks])) : 0ull;
+  }
+  if (blockIdx.x == 0 && tid < kTile && r0 + tid < rows) {
+    const int e = E[r0 + tid];
+    const bool zero = (e == OZ_EXP_EMPTY || e == OZ_EXP_NONFINITE);
+    for (int p = 0; p < ns; ++p) exps[static_cast<long long>(p) * rows + r0 + tid] = zero ? 0 : e + 1 - (p + 1) * beta;
+  }
+  __syncthreads();
+  const long long plane_elems = static_cast<long long>(rows_padded) * kp;
+#pragma unroll 1
+  for (int it = 0; it < (kTile * kTile / 8) / kThreads; ++it) {
+    const int item = tid + kThreads * it;
+    const int g = item & 7, r = item >> 3;
+    const int e = (r0 + r < rows) ? E[r0 + r] : OZ_EXP_EMPTY;
+    const bool zero = (e == OZ_EXP_EMPTY || e == OZ_EXP_NONFINITE);
+    uint64_t mag[8];  // |residual| / 2^e2
+    int e2[8];
+    bool neg[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const uint64_t b = tile[g * 8 + x][r];
+      const int ef = static_cast<int>((b >> 52) & 0x7FF);
+      const bool ok = !zero && ef != 0x7FF && (b & 0x7FFFFFFFFFFFFFFFull) != 0;
+      mag[x] = ok ? ((b & 0x000FFFFFFFFFFFFFull) | (ef ? (1ull << 52) : 0ull)) : 0ull;
+      e2[x] = (ef ? ef : 1) - 1075;
+      neg[x] = (b >> 63) != 0;
+    }
+    uint16_t* dst = planes + static_cast<long long>(r0 + r) * kp + k0 + g * 8;
+#pragma unroll 1
+    for (int p = 0; p < ns; ++p) {
+      const int ex = e + 1 - (p + 1) * beta;  // grid exponent of slice p
+      uint32_t w[4];
+#pragma unroll
+      for (int x2 = 0; x2 < 4; ++x2) {
+        int v[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int x = 2 * x2 + h;
+          // residual r = (-1)^neg mag 2^e2; slice = sign(r) RNE(mag / 2^sh); r -= slice 2^ex
+          const int sh = ex - e2[x];
+          if (sh <= 0) {  // the grid is as fine as the element's last bit: the rest is the slice
+            const uint64_t qq = (-sh < 64) ? (mag[x] << (-sh)) : 0ull;
+            v[h] = neg[x] ? -static_cast<int>(qq) : static_cast<int>(qq);
+            mag[x] = 0;
+          } else if (sh >= 64) {
+            v[h] = 0;
+          } else {
+            const uint64_t a = mag[x];
+            uint64_t qq = a >> sh;
+            const uint64_t rem = a & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+            if (rem > half || (rem == half && (qq & 1ull))) ++qq;  // round half to even
+            v[h] = neg[x] ? -static_cast<int>(qq) : static_cast<int>(qq);
+            const uint64_t sub = qq << sh;
+            if (sub > a) {  // rounded up: the residual changes sign
+              mag[x] = sub - a;
+              neg[x] = !neg[x];
+            } else {
+              mag[x] = a - sub;
+            }
+          }
+        }
+        const float f0 = __int_as_float(0x4B000080 + v[0]) - 8388736.0f;  // exact: |v| <= 2^(beta-1)
+        const float f1 = __int_as_float(0x4B000080 + v[1]) - 8388736.0f;
+        w[x2] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
+      }
+      *reinterpret_cast<uint4*>(dst + p * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// v 2^e as a double, equal to ldexp(double(v), e): for a normal result the bits are built
+// with integer operations (|v| < 2^32 fits the 53-bit significand exactly); results in the
+// subnormal or overflow range take ldexp itself.  Keeps the FP64 units for the additions.
+__device__ __forceinline__ double scaled_int(int v, int e) {
+  if (v == 0) return 0.0;
+  const uint32_t a = v < 0 ? 0u - static_cast<uint32_t>(v) : static_cast<uint32_t>(v);
+  const int L = 32 - __clz(static_cast<int>(a));  // a in [2^(L-1), 2^L)
+  const int E = L - 1 + e;                        // exponent of the leading bit
+  if (E < -1022 || E > 1023) return ldexp(static_cast<double>(v), e);
+  const uint64_t frac = (static_cast<uint64_t>(a) << (53 - L)) & ((1ull << 52) - 1);
+  const uint64_t bits = (static_cast<uint64_t>(E + 1023) << 52) | frac | (v < 0 ? (1ull << 63) : 0ull);
+  return __longlong_as_double(static_cast<long long>(bits));
+}
+
 // C_ij = sum, in order, over the terms -- single pair products (RN), or batches of the
 // pair products of one group summed in INT32 (EF, Hybrid) -- of ldexp(term, exA[ip][i] +
 // exB[jp][j]), (ip, jp) the term's (first) pair: one FP64 addition per term.
@@ -228,7 +339,7 @@ __global__ void __launch_bounds__(256) ozaki1_accumulate_kernel(int m, int n, in
       int v = 0;  // a batch's INT32 sum is exact (at most r products)
       for (int t = first; t < last; ++t) v += __ldg(p + t * plane);
       const int e = __ldg(exA + c.a_plane[first] * m + i) + __ldg(exB + c.b_plane[first] * n + j);
-      acc = __dadd_rn(acc, ldexp(static_cast<double>(v), e));
+      acc = __dadd_rn(acc, scaled_int(v, e));
     }
     C[i + j * ldc] = acc;
   }
@@ -315,10 +426,10 @@ Layout1 layout1(int m, int n, int k, int s, int variant) {
   L.kp = static_cast<int>(roundup(k, kPadK));
   L.nprod = s * (s + 1) / 2;  // one INT32 plane per pair product
   size_t off = 0;
-  L.off_RA = off;  // residuals (RN, Hybrid); the bitmask split needs none
-  if (variant != OZ_OZAKI1_EF) off = a256(off + 8ull * m * k);
+  L.off_RA = off;  // residuals (RN only: the EF and Hybrid splits take one pass)
+  if (variant == OZ_OZAKI1_RN) off = a256(off + 8ull * m * k);
   L.off_RB = off;
-  if (variant != OZ_OZAKI1_EF) off = a256(off + 8ull * k * n);
+  if (variant == OZ_OZAKI1_RN) off = a256(off + 8ull * k * n);
   L.off_EA = off;  // two row-maximum arrays per operand (current, next)
   off = a256(off + 8ull * m);
   L.off_EB = off;
@@ -352,6 +463,19 @@ cudaError_t launch_pass(bool rows_contig, int rows, int k, const double* Rin, lo
   else
     rn_split_pass_kernel<false><<<grid, kThreads, 0, st>>>(rows, k, Rin, rs_in, ks_in, Rout, rs_out, ks_out, E,
                                                            shift, beta, plane, kp, ex_out, E_next);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hybrid(bool rows_contig, int rows, int k, const double* X, long long rs, long long ks,
+                          const int32_t* E, int s, int beta, uint16_t* planes, int rows_padded, int kp,
+                          int32_t* exps, cudaStream_t st) {
+  dim3 grid(kp / kTile, rows_padded / kTile);
+  if (rows_contig)
+    hybrid_split_kernel<true><<<grid, kThreads, 0, st>>>(rows, k, X, rs, ks, E, s, beta, planes, rows_padded, kp,
+                                                         exps);
+  else
+    hybrid_split_kernel<false><<<grid, kThreads, 0, st>>>(rows, k, X, rs, ks, E, s, beta, planes, rows_padded, kp,
+                                                          exps);
   return cudaGetLastError();
 }
 
@@ -447,10 +571,21 @@ int ozaki1_split_ex(int m, int n, int k, const double* A, int lda, const double*
       return OZ_ECUDA;
     return OZ_OK;
   }
-  // RN and Hybrid: one rounding pass per slice.  RN takes each slice's grid from the
-  // current residual's row maximum; Hybrid keeps the input's and lowers it by beta per slice.
-  const bool hybrid = (variant == OZ_OZAKI1_HYBRID);
   if (launch_exponents(m, n, k, A, lda, B, ldb, EA[0], EB[0], stream) != cudaSuccess) return OZ_ECUDA;
+  if (variant == OZ_OZAKI1_HYBRID) {
+    // fixed grids from the input's row maxima: all s slices in one pass
+    if (A && m > 0 &&
+        launch_hybrid(true, m, k, A, 1, lda, EA[0], num_slices, beta, A_planes, L.mp, L.kp, A_exps, stream) !=
+            cudaSuccess)
+      return OZ_ECUDA;
+    if (B && n > 0 &&
+        launch_hybrid(false, n, k, B, ldb, 1, EB[0], num_slices, beta, B_planes, L.np, L.kp, B_exps, stream) !=
+            cudaSuccess)
+      return OZ_ECUDA;
+    return OZ_OK;
+  }
+  // RN: one rounding pass per slice, each slice's grid from the current residual's row maximum
+  const bool hybrid = false;
   for (int p = 0; p < num_slices; ++p) {
     const bool last = (p == num_slices - 1);
     const int cur = hybrid ? 0 : (p & 1), nxt = cur ^ 1;

@@ -197,10 +197,10 @@ def test_ozaki1_variant_workspace_and_errors(oz):
     lib, null = oz._lib, None
     m, n, k = 300, 520, 2100
     assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn") == oz.ozaki1_workspace_bytes(m, n, k, 7)
-    # EF needs no residual arrays
+    # EF and Hybrid split in one pass: no residual arrays
     assert oz.ozaki1_split_scratch_bytes_ex(m, n, k, "ef") < oz.ozaki1_split_scratch_bytes_ex(m, n, k, "rn")
     assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "ef") < oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn")
-    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "hybrid") == oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "rn")
+    assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "hybrid") == oz.ozaki1_workspace_bytes_ex(m, n, k, 7, "ef")
     assert oz.ozaki1_workspace_bytes_ex(m, n, k, 7, 3) == 0
     assert lib.ozaki1_dgemm_ex(8, 4, 4, 1, 8, 1, 4, 1, 8, 7, 3, null) == oz.OZ_EINVAL
     assert lib.ozaki1_dgemm_ex_ws(8, 8, 8, 1, 8, 1, 8, 1, 8, 7, 1, 256, 16, null) == oz.OZ_ENOMEM
