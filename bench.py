@@ -368,6 +368,37 @@ def run_ours(args, world, rank, local):
                               "exponents_ms": float(np.mean([e[0].elapsed_time(e[1]) for e in vev])), "steps": 3}
             del ews
 
+    # ---- the secondary path on its own workload: Scheme I, m = n = k = 4096, 7 slices
+    scheme1 = {}
+    if not args.no_variants:
+        m1 = 4096
+        A1, B1 = hpl_like(m1, m1, m1, phi=PHI, seed=SEED)
+        dA1 = torch.from_numpy(A1.T.copy()).to(device).t()
+        dB1 = torch.from_numpy(B1.T.copy()).to(device).t()
+        dC1 = torch.empty((m1, m1), dtype=torch.float64, device=device).t()
+        for name in ("rn", "ef", "hybrid"):
+            v = oz.OZAKI1_VARIANTS[name]
+            ws1 = torch.empty(oz.ozaki1_workspace_bytes_ex(m1, m1, m1, 7, v), dtype=torch.uint8, device=device)
+
+            def s1():
+                rc = lib.ozaki1_dgemm_ex_ws(m1, m1, m1, ptr(dA1), m1, ptr(dB1), m1, ptr(dC1), m1, 7, v, ptr(ws1),
+                                            ws1.numel(), sh)
+                if rc:
+                    raise RuntimeError(f"ozaki1 {name} call failed: {rc}")
+
+            s1()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                s1()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            ms = e0.elapsed_time(e1) / 5
+            scheme1[name] = {"ms_per_call": ms, "value": 2.0 * m1**3 / (ms * 1e-3) / 1e12, "unit": UNIT}
+            del ws1
+        scheme1["workload"] = "ozaki1_dgemm_ex m=n=k=4096, 7 slices, phi=0.5 (seed 0), 5 calls each"
+        del dA1, dB1, dC1
+
     # ---- end to end through the C ABI with pinned HOST buffers
     hA = torch.from_numpy(A_np.T.copy()).pin_memory()   # column-major A as a (k, m) row-major block
     hB = torch.from_numpy(B_np.T.copy()).pin_memory()
@@ -422,6 +453,7 @@ def run_ours(args, world, rank, local):
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "no flush: inputs (2 GiB each) and planes are far larger than L2"},
             "roofline": roofline, "phases": phases, "e2e": e2e, "scaling_variants": variants,
+            "scheme1_4096": scheme1,
             "cpu_baseline": cpu_baseline_measure() if not args.no_cpu_baseline else None,
             "gpu_launches": KERNELS_PER_STEP * args.steps,
             "clocks": clk, "context": context,
