@@ -10,10 +10,11 @@
 //
 // GPU mapping:
 //   * rn_split_pass (one launch per slice and operand): reads the residual tile,
-//     rounds it to the slice grid with the same IEEE double operations, writes the
-//     new residual, the slice as a bf16 plane row (K contiguous, exact: |slice| <= 64)
-//     and the row maximum of the new residual for the next pass (atomicMax of
-//     ceil(log2 |.|));
+//     rounds it to the slice grid exactly as the magic-constant double operations do
+//     (round half to even, done on the integer significand so the few FP64 units are not
+//     needed), writes the new residual, the slice as a bf16 plane row (K contiguous, exact:
+//     |slice| <= 64) and the row maximum of the new residual for the next pass (atomicMax
+//     of ceil(log2 |.|));
 //   * the slice products run on the tcgen05 engine in exact mode (oz_gemm.cu);
 //   * ozaki1 accumulation: one thread per output element, the s(s+1)/2 exact terms
 //     added in the fixed order with double-precision round-to-nearest additions.
@@ -28,21 +29,52 @@ namespace oz {
 constexpr int kTile = 64;
 constexpr int kThreads = 256;
 
-// 1.5 * 2^(52 + ex) = 0.75 * 2^53 * 2^ex, the rounding constant of the grid 2^ex.
-__device__ __forceinline__ double sigma_of(int ex) {
-  return __longlong_as_double(static_cast<long long>((static_cast<uint64_t>(1075 + ex) << 52) | (1ull << 51)));
+// (-1)^neg mag 2^e2 as a double (mag < 2^53, e2 >= -1074: always representable); +0 for mag = 0.
+__device__ __forceinline__ double compose_double(bool neg, uint64_t mag, int e2) {
+  if (mag == 0) return 0.0;
+  const int L = 64 - __clzll(static_cast<long long>(mag));
+  const int E = e2 + L - 1;  // exponent of the leading bit
+  uint64_t bits = (E >= -1022) ? ((static_cast<uint64_t>(E + 1023) << 52) | ((mag << (53 - L)) & ((1ull << 52) - 1)))
+                               : (mag << (e2 + 1074));  // subnormal
+  if (neg) bits |= 1ull << 63;
+  return __longlong_as_double(static_cast<long long>(bits));
 }
 
-// The integer S / 2^ex of a double S that is an exact multiple of 2^ex with |S / 2^ex| <= 2^52.
-__device__ __forceinline__ int slice_int(double S, int ex) {
-  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(S));
+// x rounded to the grid 2^ex, ties to even, as fl(x + sigma) - sigma does with
+// sigma = 0.75 2^53 2^ex for |x| < 2^51 2^ex: the slice integer and the exact remainder
+// x - slice 2^ex, on the integer significand (no floating-point operations).  A zero x
+// keeps its sign in the remainder, as x - (+0) does.
+__device__ __forceinline__ void rn_to_grid(double x, int ex, int& slice, double& rem) {
+  const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x));
   const int ef = static_cast<int>((b >> 52) & 0x7FF);
-  if ((b & 0x7FFFFFFFFFFFFFFFull) == 0) return 0;
-  const uint64_t mant = (b & 0x000FFFFFFFFFFFFFull) | (ef ? (1ull << 52) : 0ull);
-  const int e2 = (ef ? ef : 1) - 1075;  // S = mant * 2^e2
+  uint64_t mag = (b & 0x000FFFFFFFFFFFFFull) | (ef ? (1ull << 52) : 0ull);
+  if (mag == 0) {
+    slice = 0;
+    rem = x;
+    return;
+  }
+  const int e2 = (ef ? ef : 1) - 1075;
+  bool neg = (b >> 63) != 0;
   const int sh = ex - e2;
-  const int64_t v = static_cast<int64_t>(sh >= 0 ? (mant >> sh) : (mant << (-sh)));
-  return static_cast<int>((b >> 63) ? -v : v);
+  uint64_t qq = 0;
+  const bool sneg = neg;
+  if (sh <= 0) {
+    qq = (-sh < 64) ? (mag << (-sh)) : 0ull;
+    mag = 0;
+  } else if (sh < 64) {
+    qq = mag >> sh;
+    const uint64_t r = mag & ((1ull << sh) - 1), half = 1ull << (sh - 1);
+    if (r > half || (r == half && (qq & 1ull))) ++qq;  // round half to even
+    const uint64_t sub = qq << sh;
+    if (sub > mag) {  // rounded up: the remainder changes sign
+      mag = sub - mag;
+      neg = !neg;
+    } else {
+      mag -= sub;
+    }
+  }
+  slice = sneg ? -static_cast<int>(qq) : static_cast<int>(qq);
+  rem = compose_double(neg, mag, e2);
 }
 
 template <bool kRowsContiguous>
@@ -75,13 +107,7 @@ __global__ void __launch_bounds__(kThreads) rn_split_pass_kernel(int rows, int K
       const double x = Rin[gr * rs_in + gk * ks_in];
       const int Er = __ldg(E + gr);
       double rem = x;
-      if (Er != OZ_EXP_EMPTY) {
-        const int ex = Er - shift + 1 - beta;
-        const double sigma = sigma_of(ex);
-        const double S = __dsub_rn(__dadd_rn(x, sigma), sigma);  // x rounded to the grid 2^ex
-        sl = slice_int(S, ex);
-        rem = __dsub_rn(x, S);                                    // exact
-      }
+      if (Er != OZ_EXP_EMPTY) rn_to_grid(x, Er - shift + 1 - beta, sl, rem);  // x rounded to the grid 2^ex
       if (Rout) Rout[gr * rs_out + gk * ks_out] = rem;
       code = ceil_log2_code(rem);
     }
