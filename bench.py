@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -66,7 +67,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int, tag: str = ""):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks{tag}_rank{gpu_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"ozaki_bench_clocks{tag}_rank{gpu_index}.csv")
 
     def start(self):
         try:

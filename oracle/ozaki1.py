@@ -5,7 +5,7 @@ algorithm (the triangular loop i + j <= s + 1), the RN split of Uchino et al.
 (beta, mu, sigma = 0.75 * 2^53 * mu) and the magic-constant rounding
 paragraph; [Ozaki II, §2] for the GEMM-count table.
 
-What this oracle computes (readings listed in the design doc):
+What this oracle computes (the readings taken where the notes leave a step open):
 
 * slice width beta = min(7, floor((31 - log2 q) / 2)) with log2 taken real
   valued (RN split, step 1);

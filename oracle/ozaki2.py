@@ -15,7 +15,7 @@ scaling.  :func:`ozaki2_dgemm` reaches it the method's way (residues, one exact
 product per modulus, CRT, range reduction) and :func:`direct_dgemm` reaches it
 from the definition; tests require both to agree.
 
-Readings taken where the pages leave a step open (each is listed in the design doc):
+Readings taken where the pages leave a step open:
 
 * moduli: the greedy descending pairwise-coprime list starting at 256
   ([Ozaki II, §6] only fixes 2 <= m_t <= 256 and pairwise coprimality);
