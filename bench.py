@@ -442,6 +442,28 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(device)
         context["cublas_dgemm_tflops"] = flops / (s0.elapsed_time(s1) * 1e-3) / 1e12
         del x, y
+        # cuBLAS INT8 and BF16 GEMMs at 8192^3: the tensor rates an INT8 residue product could
+        # use on this GPU against the bf16 path the library uses
+        n8 = 8192
+        ai = torch.randint(-128, 128, (n8, n8), dtype=torch.int8, device=device)
+        bi = torch.randint(-128, 128, (n8, n8), dtype=torch.int8, device=device).t().contiguous().t()
+        ab = ai.to(torch.bfloat16)
+        bb = bi.to(torch.bfloat16)
+        for name, fn in (("cublas_int8_gemm_tops_8192", lambda: torch._int_mm(ai, bi)),
+                         ("cublas_bf16_gemm_tflops_8192", lambda: torch.matmul(ab, bb))):
+            try:
+                fn()
+                torch.cuda.synchronize(device)
+                s0.record(stream)
+                for _ in range(5):
+                    fn()
+                s1.record(stream)
+                torch.cuda.synchronize(device)
+                context[name] = 5 * 2.0 * n8**3 / (s0.elapsed_time(s1) * 1e-3) / 1e12
+            except RuntimeError as ex:  # an INT8 GEMM the installed cuBLAS lacks
+                context[name] = f"unavailable: {ex}"[:120]
+        context["cuda"] = torch.version.cuda
+        del ai, bi, ab, bb
 
     if rank == 0:
         line = {
