@@ -463,6 +463,9 @@ def run_ours(args, world, rank, local):
             except RuntimeError as ex:  # an INT8 GEMM the installed cuBLAS lacks
                 context[name] = f"unavailable: {ex}"[:120]
         context["cuda"] = torch.version.cuda
+        if isinstance(context.get("cublas_int8_gemm_tops_8192"), float):
+            # exact INT8-residue products per second of the residue GEMM against cuBLAS's INT8 GEMM
+            context["residue_gemm_vs_cublas_int8"] = achieved / context["cublas_int8_gemm_tops_8192"]
         del ai, bi, ab, bb
 
     if rank == 0:
