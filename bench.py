@@ -233,9 +233,23 @@ def cpu_baseline_measure():
     t0 = time.perf_counter()
     O.ozaki2_dgemm(A, B, S, keep=False)
     dt = time.perf_counter() - t0
-    return {"value": 2.0 * ms * ns * K / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"one oracle ozaki2_dgemm on a {ms}x{ns}x{K} block of the workload (s={S}, phi={PHI}), "
-                      f"{dt:.1f} s; numpy float64 BLAS for the per-modulus products, Python integers for the CRT"}
+    out = {"value": 2.0 * ms * ns * K / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"one oracle ozaki2_dgemm on a {ms}x{ns}x{K} block of the workload (s={S}, phi={PHI}), "
+                     f"{dt:.1f} s; numpy float64 BLAS for the per-modulus products, Python integers for the CRT"}
+    # the same oracle on one core (BLAS threads pinned to one before numpy loads), smaller block
+    code = ("import time,sys; sys.path.insert(0, %r)\n"
+            "from fp64_gemm_emulation_gb300.inputs import hpl_like\nfrom oracle import ozaki2 as O\n"
+            "A, B = hpl_like(256, 256, %d, phi=%r, seed=%d)\nt0 = time.perf_counter()\n"
+            "O.ozaki2_dgemm(A, B, %d, keep=False)\nprint(time.perf_counter() - t0)\n") % (ROOT, K, PHI, SEED, S)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+        dt1 = float(r.stdout.strip().splitlines()[-1])
+        out["one_core"] = {"value": 2.0 * 256 * 256 * K / dt1 / 1e12, "unit": UNIT, "cores": 1,
+                           "sample": f"256x256x{K} block, {dt1:.1f} s"}
+    except (subprocess.SubprocessError, ValueError, IndexError) as ex:
+        out["one_core"] = f"unavailable: {ex}"[:120]
+    return out
 
 
 def run_ours(args, world, rank, local):
