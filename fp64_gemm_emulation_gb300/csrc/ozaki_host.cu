@@ -747,8 +747,9 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
   // release the workspace after the copies out, then wait for everything
   cudaEvent_t done = nullptr;
   if (ws) {
-    if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess && cudaEventRecord(done, sout) == cudaSuccess)
-      cudaStreamWaitEvent(scomp, done, 0);
+    const bool ordered = cudaEventCreateWithFlags(&done, cudaEventDisableTiming) == cudaSuccess &&
+                         cudaEventRecord(done, sout) == cudaSuccess && cudaStreamWaitEvent(scomp, done, 0) == cudaSuccess;
+    if (!ordered) cudaStreamSynchronize(sout);  // the copies out read the workspace: finish them first
     cudaFreeAsync(ws, scomp);
   }
   if (cudaStreamSynchronize(sin) != cudaSuccess && !rc) rc = OZ_ECUDA;
