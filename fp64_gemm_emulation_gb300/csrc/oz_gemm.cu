@@ -69,8 +69,9 @@ __device__ int g_status = 0;
 // producer adds 1 to its launch's counter and compares its own count with the pairs'
 // average (the counter value it loaded at the previous checkpoint, so the load latency is
 // hidden); a producer more than kPaceWindow checkpoints ahead pauses, for at most
-// kPaceLimitNs.  Pairs that share plane panels then stream them at about the same time,
-// so the panels are read from DRAM once and served to the others from L2.  A finished
+// kPaceLimitNs (a pair whose pause runs out stops pausing for the rest of the launch: its
+// peers are not all resident).  Pairs that share plane panels then stream them at about the
+// same time, so the panels are read from DRAM once and served to the others from L2.  A finished
 // pair adds a large credit so the tail of the launch never waits.  The counter slot of
 // a launch is zeroed on its stream just before it starts.
 constexpr int kPaceSlots = 64;
@@ -267,7 +268,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      const bool pacer = (rank == 0);
+      const bool pacer = (rank == 0);  // the leader's producer counts the pair's progress
+      bool may_pause = pacer;          // cleared once a pause runs out (see below)
       unsigned int* ctr = &g_pace_ctr[c.launch_id % kPaceSlots];
       uint32_t paced = 0, checkpoints = 0, seen = 0;
       for (int idx = 0; idx < sched.count() && !*abort_flag; ++idx) {
@@ -297,12 +299,16 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             ++checkpoints;
             atomicAdd(ctr, 1u);
             const uint32_t np = static_cast<uint32_t>(sched.npairs);
-            if (checkpoints * np > seen + kPaceWindow * np) {  // ahead of the average: pause
+            if (may_pause && checkpoints * np > seen + kPaceWindow * np) {  // ahead of the average: pause
               const uint64_t t0 = globaltimer_ns();
               while (checkpoints * np > seen + kPaceWindow * np && globaltimer_ns() - t0 < kPaceLimitNs) {
                 __nanosleep(256);
                 seen = *reinterpret_cast<volatile unsigned int*>(ctr);
               }
+              // Still ahead after the limit: some pairs of this launch are not running (another
+              // kernel holds their SMs), so the average cannot catch up.  Stop pausing for the
+              // rest of the launch; the pair keeps counting so the others' average stays right.
+              if (checkpoints * np > seen + kPaceWindow * np) may_pause = false;
             }
             seen = *reinterpret_cast<volatile unsigned int*>(ctr);  // used at the next checkpoint
           }

@@ -246,3 +246,21 @@ def test_host_pipeline_four_by_two_blocks(oz):
     assert rc == 0
     ref = host(oz.ozaki2_dgemm(dev(A), dev(B), 14))
     assert np.array_equal(bits(Ch), bits(ref))
+
+
+def test_concurrent_calls_on_two_streams(oz):
+    # two products at once on two streams (the second launch's CTA pairs wait for SMs the first
+    # one holds): both results exact, no device-status error
+    pairs = [hpl_like(1300, 1200, 2100, phi=0.5, seed=19), hpl_like(1000, 1500, 1700, phi=2.0, seed=20)]
+    refs = [O.ozaki2_dgemm(A, B, 14, keep=False).C for A, B in pairs]
+    dev_in = [(dev(A), dev(B)) for A, B in pairs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [None, None]
+    torch.cuda.synchronize()
+    for i in range(2):
+        with torch.cuda.stream(streams[i]):
+            outs[i] = oz.ozaki2_dgemm(dev_in[i][0], dev_in[i][1], 14)
+    torch.cuda.synchronize()
+    for C, ref in zip(outs, refs):
+        assert np.array_equal(bits(host(C)), bits(ref))
+    assert oz.ozaki_get_device_status() == oz.OZ_OK
