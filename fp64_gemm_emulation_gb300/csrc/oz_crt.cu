@@ -9,7 +9,10 @@
 // The quotient estimate is biased down by 2^-8, more than its error, so it is never
 // too large and at most one too small; one correction then restores the unique
 // representative ([Ozaki II] section 5: the true product lies in (-M/2, M/2) because
-// 2 c_max < M).  The remainder and the rounding are exact integer arithmetic.
+// 2 c_max < M).  The estimate can only be one too small when its fractional part is
+// within 3 * 2^-9 of the next integer, so the comparison with M/2 that detects it runs
+// for those elements alone (X near +-M/2; none for typical products, whose |X| is far
+// below M/2).  The remainder and the rounding are exact integer arithmetic.
 #include <cmath>
 
 #include "oz_internal.h"
@@ -81,49 +84,52 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLim
   return bits | (neg ? 0x8000000000000000ull : 0ull);
 }
 
-// Fast path of the final rounding for NL-limb magnitudes: the 64 bits below the leading
-// one plus a sticky bit decide RN-even whenever the result is a normal number (or
-// overflows to infinity).  Returns false for results in the subnormal range, which the
-// general routine above handles.
+// RN-even of (-1)^neg * x * 2^-D (x: NL limbs) for results that are normal numbers or
+// overflow, from 64-bit words: the word holding the leading one and the word below it
+// give the 64-bit window, anything lower only the sticky bit.  Returns false for results
+// in the subnormal range (the general routine above handles them).
 template <int NL>
-__device__ __forceinline__ bool round_normal_bits(const uint32_t (&x)[kLimbs], bool neg, int D, uint64_t& out) {
-  int h = -1;
-  uint32_t top = 0, nx = 0, nx2 = 0;
+__device__ __forceinline__ bool round_normal_words(const uint32_t (&x)[kLimbs], bool neg, int D, uint64_t& out) {
+  constexpr int NW = (NL + 1) / 2;
+  uint64_t w[NW];
 #pragma unroll
-  for (int l = NL - 1; l >= 0; --l) {
-    if (h < 0 && x[l] != 0) {
-      h = l;
-      top = x[l];
-      nx = (l >= 1) ? x[l - 1] : 0u;
-      nx2 = (l >= 2) ? x[l - 2] : 0u;
+  for (int i = 0; i < NW; ++i)
+    w[i] = static_cast<uint64_t>(x[2 * i]) | ((2 * i + 1 < NL) ? static_cast<uint64_t>(x[2 * i + 1]) << 32 : 0ull);
+  // the highest non-zero word w[h] (h = 0 if all above w[0] are zero), the word below it, and
+  // whether any word further down is non-zero
+  uint64_t hi = w[0], lo = 0, below = 0;
+  int base = 0;
+#pragma unroll
+  for (int i = 1; i < NW; ++i) {
+    if (w[i] != 0) {
+      hi = w[i];
+      lo = w[i - 1];
+      base = 64 * i;
+      below = 0;
+#pragma unroll
+      for (int b = 0; b + 1 < i; ++b) below |= w[b];
     }
   }
-  if (h < 0) {
+  bool sticky = below != 0;
+  if (hi == 0) {
     out = 0;  // exact zero: +0.0
     return true;
   }
-  bool sticky = false;
-#pragma unroll
-  for (int l = 0; l < NL; ++l) sticky |= (l <= h - 3) && (x[l] != 0u);
-  const int lz = __clz(top);
-  uint64_t w = (static_cast<uint64_t>(top) << 32 | nx) << lz;
-  if (lz) {
-    w |= nx2 >> (32 - lz);
-    sticky |= (nx2 << lz) != 0u;
-  } else {
-    sticky |= nx2 != 0u;
-  }
-  const int e_unb = (32 * h + 31 - lz) - D;  // exponent of the leading one in the result
+  const int lz = __clzll(static_cast<long long>(hi));
+  const uint64_t win = lz ? (hi << lz) | (lo >> (64 - lz)) : hi;
+  sticky = sticky || ((lz ? (lo << lz) : lo) != 0);
+  const int e_unb = base + 63 - lz - D;  // exponent of the leading one in the result
   if (e_unb < -1022) return false;
+  const uint64_t sgn = neg ? 0x8000000000000000ull : 0ull;
   if (e_unb > 1023) {
-    out = 0x7FF0000000000000ull | (neg ? 0x8000000000000000ull : 0ull);
+    out = 0x7FF0000000000000ull | sgn;
     return true;
   }
-  uint64_t mant = w >> 11;
-  const bool rb = (w >> 10) & 1u;
-  sticky |= (w & 0x3FFu) != 0u;
+  uint64_t mant = win >> 11;
+  const bool rb = (win >> 10) & 1u;
+  sticky = sticky || ((win & 0x3FFu) != 0);
   if (rb && (sticky || (mant & 1u))) ++mant;  // may carry into 2^53: exponent + 1 below
-  out = ((static_cast<uint64_t>(e_unb + 1022) << 52) + mant) | (neg ? 0x8000000000000000ull : 0ull);
+  out = ((static_cast<uint64_t>(e_unb + 1022) << 52) + mant) | sgn;
   return true;
 }
 
@@ -188,11 +194,16 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
       }
       // Q = floor(Z/M + 1/2 - 2^-8) from the top three limbs in FP32 (error < 2^-9):
       // round(Z/M) or one less, never more, so X = Z - Q M is the representative or
-      // the representative plus M.
+      // the representative plus M.  It is one less only if the estimate h lies within
+      // 2^-9 + 2^-8 of the next integer, so below a fractional part of 1 - 2^-7 it is
+      // exactly round(Z/M) and X needs no correction.
       float zs = __uint2float_rn(x[NL - 1]);
       zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, zs);
       zs = fmaf(__uint2float_rn(x[NL - 3]), 5.421010862427522e-20f, zs);
-      const uint32_t Q = __float2uint_rd(fmaf(zs, inv_m_top, 0.49609375f));
+      const float h = fmaf(zs, inv_m_top, 0.49609375f);
+      const float hq = floorf(h);
+      const bool near = (h - hq) >= 0.9921875f;  // exact difference: h < 2^13
+      const uint32_t Q = static_cast<uint32_t>(hq);
       uint64_t qc = 0;
       uint32_t borrow = 0;
 #pragma unroll
@@ -204,15 +215,17 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         borrow = static_cast<uint32_t>(d >> 63);
       }
       bool neg = (x[NL - 1] >> 31) != 0;
-      if (neg) {  // X is the (negative) representative: take its magnitude
-        uint32_t cy = 1;
+      {  // magnitude: X for X >= 0, two's complement negation otherwise
+        const uint32_t flip = neg ? 0xFFFFFFFFu : 0u;
+        uint32_t cy = neg ? 1u : 0u;
 #pragma unroll
         for (int l = 0; l < NL; ++l) {
-          const uint64_t v = static_cast<uint64_t>(~x[l]) + cy;
+          const uint64_t v = static_cast<uint64_t>(x[l] ^ flip) + cy;
           x[l] = static_cast<uint32_t>(v);
           cy = static_cast<uint32_t>(v >> 32);
         }
-      } else {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
+      }
+      if (near && !neg) {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
         bool gt = false, decided = false;
 #pragma unroll
         for (int l = NL - 1; l >= 0; --l) {
@@ -236,7 +249,7 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
       for (int l = NL; l < kLimbs; ++l) x[l] = 0;
       const int D = 2 * c.kA - E[e] - F;  // d_i + e_j
       uint64_t bits;
-      if (!round_normal_bits<NL>(x, neg, D, bits)) bits = round_scaled_bits(x, neg, D);
+      if (!round_normal_words<NL>(x, neg, D, bits)) bits = round_scaled_bits(x, neg, D);
       out[e] = __longlong_as_double(static_cast<long long>(bits));
     }
   }
