@@ -25,6 +25,8 @@ struct SplitConsts {
   uint32_t c16[kMaxModuli];     // 2^16 mod m
   uint32_t c32[kMaxModuli];     // 2^32 mod m
   uint32_t c48[kMaxModuli];     // 2^48 mod m
+  uint32_t c64[kMaxModuli];     // 2^64 mod m
+  uint32_t c80[kMaxModuli];     // 2^80 mod m
   uint32_t magic[kMaxModuli];   // ceil(2^39 / m): y mod m for y < 2^30
   int shift_ok;                 // every modulus m has m 2^22 > 2^26 (the shifted path's bound)
 };

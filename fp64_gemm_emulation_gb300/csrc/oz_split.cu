@@ -99,6 +99,33 @@ __device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_
 // (SplitConsts::shift_ok), and ys < 2^31 <= 2^39 / m keeps the quotient exact.
 constexpr uint32_t kShiftMax = 10;
 
+// Wide path (kShiftMax < p <= kWideMax for some element: k_A above 62, e.g. 17 or more
+// moduli, or 16 moduli with a small k): a' = u 2^p < 2^96 as six signed 16-bit limbs.  Each
+// constant 2^(16 i) mod m is below m, so |y| < 6 2^16 m < BIG = m 2^22 and
+// ys < m 2^23 <= 2^31: the single Barrett step stays exact for every modulus.  Every a' the
+// scalings produce is below 2^(k_A + 1) <= 2^86 for 20 moduli, so p never exceeds kWideMax.
+constexpr uint32_t kWideMax = 43;
+
+__device__ __forceinline__ float residue_wide(uint64_t packed, uint32_t m, const uint32_t (&cw)[6], uint32_t magic,
+                                              uint32_t big, uint32_t halfm, uint32_t fbase) {
+  // the limbs are rebuilt for every modulus: this path is rare, and holding them for all
+  // eight values would raise the register count of the common paths
+  const uint64_t u = packed & ((1ull << 53) - 1);
+  const uint32_t p = static_cast<uint32_t>(packed >> 53) & 0x3FFu;
+  const uint64_t lo = u << p;                                            // bits 0..63
+  const uint32_t hi = p ? static_cast<uint32_t>(u >> (64 - p)) : 0u;     // bits 64..95
+  int acc = static_cast<int>(static_cast<uint32_t>(lo) & 0xFFFFu);
+  acc += static_cast<int>(static_cast<uint32_t>(lo) >> 16) * static_cast<int>(cw[1]);
+  acc += static_cast<int>(static_cast<uint32_t>(lo >> 32) & 0xFFFFu) * static_cast<int>(cw[2]);
+  acc += static_cast<int>(static_cast<uint32_t>(lo >> 48)) * static_cast<int>(cw[3]);
+  acc += static_cast<int>(hi & 0xFFFFu) * static_cast<int>(cw[4]);
+  acc += static_cast<int>(hi >> 16) * static_cast<int>(cw[5]);
+  const bool neg = (packed >> 63) != 0;
+  const uint32_t ys = (neg ? big - static_cast<uint32_t>(acc) : static_cast<uint32_t>(acc)) + halfm;
+  const uint32_t q = __umulhi(ys, magic) >> 7;
+  return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
+}
+
 __device__ __forceinline__ float residue_shifted(int sx0, int sx1, int sx2, int sx3, uint32_t negf, uint32_t m,
                                                  uint32_t c16, uint32_t c32, uint32_t c48, uint32_t magic,
                                                  uint32_t big, uint32_t halfm, uint32_t fbase) {
@@ -126,15 +153,12 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
     pp[x] = static_cast<uint32_t>(v[x] >> 53) & 0x3FFu;
     ng[x] = (v[x] >> 63) != 0;
   }
-  bool any_p = false, big_p = false;
+  uint32_t pmax = 0;
 #pragma unroll
-  for (int x = 0; x < 8; ++x) {
-    any_p |= (pp[x] != 0);
-    big_p |= (pp[x] > kShiftMax);
-  }
-  const bool warp_any_p = __any_sync(0xFFFFFFFFu, any_p);
-  const bool warp_big_p = __any_sync(0xFFFFFFFFu, big_p);
-  if (warp_any_p && !warp_big_p && c.shift_ok) {
+  for (int x = 0; x < 8; ++x) pmax = max(pmax, pp[x]);
+  pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
+  const bool warp_any_p = pmax != 0;
+  if (warp_any_p && pmax <= kShiftMax && c.shift_ok) {
     // every a' of the warp is u 2^p with p <= kShiftMax: four signed 16-bit limbs of u 2^p
     int sx0[8], sx1[8], sx2[8], sx3[8];
     uint32_t nf[8];
@@ -160,6 +184,22 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
                                          c48, mg, big, halfm, fbase);
         const float hi = residue_shifted(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], sx3[2 * x + 1],
                                          nf[2 * x + 1], m, c16, c32, c48, mg, big, halfm, fbase);
+        w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
+      }
+      if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else if (warp_any_p && pmax <= kWideMax) {
+    // some a' of the warp is u 2^p with kShiftMax < p <= kWideMax: six 16-bit limbs
+#pragma unroll 1
+    for (int t = 0; t < c.s; ++t) {
+      const uint32_t m = static_cast<uint32_t>(c.mod[t]), mg = c.magic[t];
+      const uint32_t cw[6] = {1u, c.c16[t], c.c32[t], c.c48[t], c.c64[t], c.c80[t]};
+      const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
+      uint32_t w[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float lo = residue_wide(v[2 * x], m, cw, mg, big, halfm, fbase);
+        const float hi = residue_wide(v[2 * x + 1], m, cw, mg, big, halfm, fbase);
         w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
       }
       if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -253,7 +293,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, c
 // K-contiguous operand (B, column j = k contiguous): no transpose needed.  One thread
 // takes 8 consecutive k of one row: 64 contiguous bytes in, 16 contiguous bytes out per
 // modulus; a warp covers 256 consecutive k (2 KB read, 512 B written per plane).
-__global__ void __launch_bounds__(256) split_kcontig_kernel(int rows, int K, const double* __restrict__ X,
+__global__ void __launch_bounds__(256, 4) split_kcontig_kernel(int rows, int K, const double* __restrict__ X,
                                                             long long ld, const int32_t* __restrict__ exps,
                                                             const SplitConsts c, uint16_t* __restrict__ planes,
                                                             int rows_padded, int kp) {

@@ -153,6 +153,8 @@ int fill_split_consts(int s, long long k_inner, SplitConsts* out) {
     out->c16[t] = (1u << 16) % m;
     out->c32[t] = static_cast<uint32_t>((1ull << 32) % m);
     out->c48[t] = static_cast<uint32_t>((1ull << 48) % m);
+    out->c64[t] = static_cast<uint32_t>((static_cast<uint64_t>(out->c48[t]) * out->c16[t]) % m);
+    out->c80[t] = static_cast<uint32_t>((static_cast<uint64_t>(out->c64[t]) * out->c16[t]) % m);
     out->magic[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
   }
   return OZ_OK;

@@ -264,3 +264,76 @@ def test_concurrent_calls_on_two_streams(oz):
     for C, ref in zip(outs, refs):
         assert np.array_equal(bits(host(C)), bits(ref))
     assert oz.ozaki_get_device_status() == oz.OZ_OK
+
+
+@pytest.mark.parametrize("s", [2, 8, 14, 16, 20])
+def test_crt_on_random_residue_tuples(oz, s):
+    # Any residue tuple is a valid input of the CRT step.  With uniform residues Z/M has a
+    # uniform fractional part, so about 1 element in 128 lies near +-M/2 (the quotient
+    # estimate's corrected case), and the rows at the ends of the exponent range put the
+    # results across the subnormal and the overflow boundaries.
+    m, n, k = 301, 203, 1024
+    moduli = O.greedy_moduli(s)
+    cc = O.crt_constants(moduli)
+    kA = O.choose_k(cc.M, k)
+    bm = cc.M.bit_length()
+    rng = np.random.default_rng(1000 + s)
+    Cres = np.stack([rng.integers(0, mt, size=(m, n)) for mt in moduli])
+    E = rng.integers(-40, 41, m)
+    F = rng.integers(-40, 41, n)
+    # D = 2 kA - E - F: about bm + 1074 puts |X| 2^-D at the bottom of the subnormals,
+    # about bm - 1025 at the top of the normal range
+    E[:80] = 2 * kA - (bm + 1030) - rng.integers(-45, 46, 80)
+    E[80:140] = 2 * kA - (bm - 1026) - rng.integers(-3, 4, 60)
+    F[:40] = 0
+    E[140], E[141] = oz.OZ_EXP_EMPTY, oz.OZ_EXP_NONFINITE
+    F[50], F[51] = oz.OZ_EXP_EMPTY, oz.OZ_EXP_NONFINITE
+    X = O.crt_reconstruct(Cres, cc)
+    live_r = (E != oz.OZ_EXP_EMPTY) & (E != oz.OZ_EXP_NONFINITE)
+    live_c = (F != oz.OZ_EXP_EMPTY) & (F != oz.OZ_EXP_NONFINITE)
+    d = [int(kA - e) if ok else 0 for e, ok in zip(E, live_r)]
+    e = [int(kA - f) if ok else 0 for f, ok in zip(F, live_c)]
+    ref = O.unscale(X, d, e)
+    ref[E == oz.OZ_EXP_EMPTY, :] = 0.0
+    ref[:, F == oz.OZ_EXP_EMPTY] = 0.0
+    ref[E == oz.OZ_EXP_NONFINITE, :] = np.nan
+    ref[:, F == oz.OZ_EXP_NONFINITE] = np.nan
+    mp, np_, _ = oz.ozaki2_plane_dims(m, n, k)
+    Cr = np.zeros((s, np_, mp), dtype=np.uint8)
+    Cr[:, :n, :m] = np.transpose(Cres, (0, 2, 1))
+    rowexp = torch.from_numpy(E.astype(np.int32)).cuda()
+    colexp = torch.from_numpy(F.astype(np.int32)).cuda()
+    C = host(oz.ozaki2_crt(m, n, k, s, torch.from_numpy(Cr).cuda(), rowexp, colexp))
+    got, want = bits(C), bits(ref)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(C), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    # the sample really spans the cases: subnormal, infinite and near-M/2 results
+    fin = ref[live_r][:, live_c]
+    assert (np.abs(fin[fin != 0]) < 2.0**-1022).any() and np.isinf(fin).any()
+    near = np.abs(np.abs(X.astype(float)) / float(cc.M) - 0.5) < 2.0**-8
+    assert near.sum() > 20
+
+
+@pytest.mark.parametrize("s,k", [(20, 3000), (20, 40), (16, 16), (17, 4096)])
+def test_split_with_large_shifts(oz, s, k):
+    # k_A above 62 (17 or more moduli, or 16 with a small k) makes a' = u 2^p with p > 10
+    # (the six-limb residue path); rows and columns whose maximum is a small subnormal reach
+    # p close to k_A, past 43 at 20 moduli (the per-bit fallback)
+    m, n = 96, 72
+    A, B = hpl_like(m, n, k, phi=4.0, seed=s + k)
+    rng = np.random.default_rng(s * k)
+    A[3, :] = rng.integers(-3, 4, k) * 2.0**-1074
+    A[5, :] = rng.integers(-(2**20), 2**20, k) * 2.0**-1074
+    A[6, :] *= 2.0**-1060
+    B[:, 7] = rng.integers(-3, 4, k) * 2.0**-1074
+    B[:, 9] *= 2.0**-1050
+    ref = O.ozaki2_dgemm(A, B, s)
+    assert ref.k > 52
+    dA, dB = dev(A), dev(B)
+    rowexp, colexp = oz.ozaki2_exponents(dA, dB)
+    Ap, Bp = oz.ozaki2_split(dA, dB, s, rowexp, colexp)
+    assert np.array_equal(bf16_planes_to_int(Ap)[:, :m, :k], ref.Ares.astype(np.int64))
+    assert np.array_equal(bf16_planes_to_int(Bp)[:, :n, :k], np.transpose(ref.Bres, (0, 2, 1)).astype(np.int64))
+    C = oz.ozaki2_dgemm(dA, dB, s)
+    assert np.array_equal(bits(host(C)), bits(ref.C))
