@@ -2,7 +2,7 @@
 //
 // [Ozaki II] Algorithm 1, steps 4-6.  Per output element, with residues
 // c_t = C''_t in [0, m_t) and P_t = M_t y_t (< M, so P_t / M = y_t / m_t):
-//   Z    = sum_t c_t P_t                      exact, up to six 32-bit limbs
+//   Z    = sum_t c_t P_t                      exact: 19/20-bit limb sums, then up to six 32-bit words
 //   Q    = round(Z / M) or one less            from the top limbs of Z in FP32
 //   X    = Z - Q M, then one correction by M  symmetric representative, |X| < M/2
 //   C    = RN(X 2^-(d_i + e_j))               one rounding, subnormals included
@@ -134,13 +134,18 @@ __device__ __forceinline__ bool round_normal_words(const uint32_t (&x)[kLimbs], 
 }
 
 // One thread = 4 consecutive rows i of one column j (a 4-byte load per modulus).
-// NL = 32-bit limbs needed for Z = sum_t c_t P_t (< 255 s M).
-template <int NL>
+// NL = 32-bit limbs needed for Z = sum_t c_t P_t (< 255 s M); the sum itself runs on
+// NS limbs of LB bits (P_t split the same way), each a 32-bit accumulator: every term
+// c_t P_t[l] is below 255 2^LB and s of them stay below 2^32, so the sums are exact
+// 32-bit multiply-adds (cheaper than 32 x 32 -> 64-bit ones); the limbs are then
+// carried into NL words.
+template <int NL, int LB, int NS>
 __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c, float inv_m_top,
                                                   const uint8_t* __restrict__ C_res,
                                                   const int32_t* __restrict__ rowexp,
                                                   const int32_t* __restrict__ colexp, double* __restrict__ C,
                                                   long long ldc) {
+  static_assert(LB >= 16 && LB <= 20 && NS <= kSmallLimbs && LB * (NS - 1) < 32 * NL, "CRT limb class");
   const int i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i0 >= m) return;
   const long long plane = static_cast<long long>(np) * mp;
@@ -156,13 +161,13 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
     for (int t = 0; t < kMaxModuli; ++t)
       res[t] = (t < c.s) ? __ldg(reinterpret_cast<const uint32_t*>(base + t * plane)) : 0u;
     double* out = C + i0 + j * ldc;
-    // Z = sum_t c_t P_t for the 4 elements at once (64-bit partial limbs, carries later):
-    // each constant limb P_t[l] is read once per 4 elements
-    uint64_t acc[4][NL];
+    // Z = sum_t c_t P_t for the 4 elements at once, on LB-bit limbs (carries later):
+    // each constant limb is read once per 4 elements
+    uint32_t acc[4][NS];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
 #pragma unroll
-      for (int l = 0; l < NL; ++l) acc[e][l] = 0;
+      for (int l = 0; l < NS; ++l) acc[e][l] = 0;
 #pragma unroll
     for (int t = 0; t < kMaxModuli; ++t) {
       if (t >= c.s) break;
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
       for (int e = 0; e < 4; ++e) {
         const uint32_t r = __byte_perm(res[t], 0u, 0x4440u | static_cast<uint32_t>(e));  // byte e
 #pragma unroll
-        for (int l = 0; l < NL; ++l) acc[e][l] += static_cast<uint64_t>(r) * c.P[t][l];
+        for (int l = 0; l < NS; ++l) acc[e][l] += r * c.Ps[t][l];
       }
     }
 #pragma unroll
@@ -184,13 +189,20 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         out[e] = 0.0;
         continue;
       }
+      // Z into NL words: word w collects the limbs that start in bits [32w, 32w + 32).
+      // Two limbs at most start in one word (LB >= 16), the lower one shifted by at most
+      // 31 - LB, so run < 2^63 + 2^44 + 2^32 never overflows.
       uint32_t x[kLimbs];
-      uint64_t carry = 0;
+      uint64_t run = 0;
 #pragma unroll
-      for (int l = 0; l < NL; ++l) {
-        const uint64_t v = acc[e][l] + carry;
-        x[l] = static_cast<uint32_t>(v);
-        carry = v >> 32;
+      for (int w = 0; w < NL; ++w) {
+#pragma unroll
+        for (int l = 0; l < NS; ++l) {
+          const int pos = LB * l - 32 * w;
+          if (pos >= 0 && pos < 32) run += static_cast<uint64_t>(acc[e][l]) << pos;
+        }
+        x[w] = static_cast<uint32_t>(run);
+        run >>= 32;
       }
       // Q = floor(Z/M + 1/2 - 2^-8) from the top three limbs in FP32 (error < 2^-9):
       // round(Z/M) or one less, never more, so X = Z - Q M is the representative or
@@ -274,14 +286,23 @@ cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const u
   double Md = 0.0;
   for (int l = kLimbs - 1; l >= 0; --l) Md = Md * 4294967296.0 + c.M[l];
   const float inv_m_top = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / Md);
-  if (nl == 3)
-    crt_kernel<3><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
-  else if (nl == 4)
-    crt_kernel<4><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
-  else if (nl == 5)
-    crt_kernel<5><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
+  // (NL, LB, NS) classes: each s runs in the class of its NL and LB, with NS the class's
+  // largest limb count (unused top limbs of P_t are zero)
+#define OZ_CRT_LAUNCH(NLv, LBv, NSv) \
+  crt_kernel<NLv, LBv, NSv><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc)
+  if (nl == 3 && c.lb == 20 && c.ns <= 4)
+    OZ_CRT_LAUNCH(3, 20, 4);
+  else if (nl == 4 && c.lb == 20 && c.ns <= 6)
+    OZ_CRT_LAUNCH(4, 20, 6);
+  else if (nl == 5 && c.lb == 20 && c.ns <= 7)
+    OZ_CRT_LAUNCH(5, 20, 7);
+  else if (nl == 5 && c.lb == 19 && c.ns <= 8)
+    OZ_CRT_LAUNCH(5, 19, 8);
+  else if (nl == 6 && c.lb == 19 && c.ns <= 9)
+    OZ_CRT_LAUNCH(6, 19, 9);
   else
-    crt_kernel<6><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc);
+    return cudaErrorInvalidValue;  // no class for this moduli count (cannot happen for 2..20 moduli <= 256)
+#undef OZ_CRT_LAUNCH
   return cudaGetLastError();
 }
 
