@@ -3,8 +3,10 @@
 //
 // [Ozaki II] section 3 scales A by D = diag(2^d_i) and B by E = diag(2^e_j); the
 // exponents d_i = k_A - E_i need E_i = ceil(log2 max_j |a_ij|) = max_j ceil(log2 |a_ij|)
-// (ceil(log2 .) is monotone), which is computed exactly from the bit fields and
-// reduced with an integer max.  HBM-bound: one read of A and B.
+// (ceil(log2 .) is monotone).  The magnitude bits of an IEEE-754 double order like its
+// magnitude (subnormals, infinity and NaN included), so the kernels reduce the 63-bit
+// magnitude patterns with an integer max and take ceil(log2 .) (exactly, from the bit
+// fields) of the maximum alone.  HBM-bound: one read of A and B.
 #include "oz_fp.cuh"
 #include "oz_internal.h"
 
@@ -22,10 +24,10 @@ __global__ void __launch_bounds__(256) rowexp_colmajor_kernel(int m, int k, cons
   const int j0 = blockIdx.y * kRowExpCols;
   const int j1 = min(k, j0 + kRowExpCols);
   const double* p = A + i + static_cast<long long>(j0) * lda;
-  int best = OZ_EXP_EMPTY;
+  unsigned long long mag = 0;
 #pragma unroll 16
-  for (int j = j0; j < j1; ++j, p += lda) best = max(best, log2_code<kFloor>(__ldg(p)));
-  if (best != OZ_EXP_EMPTY) atomicMax(&rowexp[i], best);
+  for (int j = j0; j < j1; ++j, p += lda) mag = max(mag, magnitude_bits(__ldg(p)));
+  if (mag != 0) atomicMax(&rowexp[i], log2_code<kFloor>(__longlong_as_double(static_cast<long long>(mag))));
 }
 
 // B column-major (k x n): warp = one column j and a slice of kColExpRows rows.
@@ -38,9 +40,10 @@ __global__ void __launch_bounds__(256) colexp_colmajor_kernel(int k, int n, cons
   const int r0 = blockIdx.y * kColExpRows;
   const int r1 = min(k, r0 + kColExpRows);
   const double* col = B + static_cast<long long>(j) * ldb;
-  int best = OZ_EXP_EMPTY;
+  unsigned long long mag = 0;
 #pragma unroll 16
-  for (int r = r0 + lane; r < r1; r += 32) best = max(best, log2_code<kFloor>(__ldg(col + r)));
+  for (int r = r0 + lane; r < r1; r += 32) mag = max(mag, magnitude_bits(__ldg(col + r)));
+  int best = mag ? log2_code<kFloor>(__longlong_as_double(static_cast<long long>(mag))) : OZ_EXP_EMPTY;
   best = __reduce_max_sync(0xFFFFFFFFu, best);
   if (lane == 0 && best != OZ_EXP_EMPTY) atomicMax(&colexp[j], best);
 }

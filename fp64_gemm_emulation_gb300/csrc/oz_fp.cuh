@@ -7,6 +7,12 @@
 
 namespace oz {
 
+// |x| as its 63-bit pattern: for x, y not NaN, |x| < |y| iff the patterns compare the same
+// way, and every NaN pattern lies above infinity's.
+__device__ __forceinline__ unsigned long long magnitude_bits(double x) {
+  return static_cast<unsigned long long>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;
+}
+
 // ceil(log2 |x|) from the IEEE-754 fields; OZ_EXP_EMPTY for 0, OZ_EXP_NONFINITE for Inf/NaN.
 __device__ __forceinline__ int ceil_log2_code(double x) {
   const uint64_t b = static_cast<uint64_t>(__double_as_longlong(x)) & 0x7FFFFFFFFFFFFFFFull;

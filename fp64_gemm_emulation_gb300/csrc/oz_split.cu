@@ -78,17 +78,18 @@ __device__ __forceinline__ uint32_t residue_bf16(uint32_t x0, uint32_t x1, uint3
 }
 
 // Fast path (p == 0): the symmetric residue of a' = sign * u modulo m, as a float.
-//   ys = sign * (x2 c32 + x1 c16 + x0) + neg * BIG + floor(m/2)   (BIG = m 2^22 > |y|)
-//   q  = floor(ys / m)                                            (one Barrett step)
+//   ys = sign * (x2 c32 + x1 c16 + x0) + BIG + floor(m/2)   (BIG = m 2^22)
+//   q  = floor(ys / m)                                      (one Barrett step)
 //   ys - q m = v + floor(m/2) with v the symmetric representative in
 //   [-floor(m/2), ceil(m/2) - 1]; the float 2^23 + 128 + v is built directly from the
 //   bits (the per-modulus constant absorbs floor(m/2)) and 2^23 + 128 subtracted.
-// sx* are the sign-applied 16-bit limbs of u, negf is 1 for a negative a'.
-__device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_t negf, uint32_t m, uint32_t c16,
-                                              uint32_t c32, uint32_t magic, uint32_t big, uint32_t halfm,
-                                              uint32_t fbase) {
+// BIG is a multiple of m above |y| < (m - 1)(2^21 + 2^16) + 2^16, added whatever the sign,
+// so ys > 0 and ys < m 2^22 + m 2^21.05 + m < 2^31 <= 2^39 / m keeps the quotient exact.
+// sx* are the sign-applied 16-bit limbs of u; offs = BIG + floor(m/2).
+__device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_t m, uint32_t c16, uint32_t c32,
+                                              uint32_t magic, uint32_t offs, uint32_t fbase) {
   const uint32_t y = static_cast<uint32_t>(sx2 * static_cast<int>(c32) + sx1 * static_cast<int>(c16) + sx0);
-  const uint32_t ys = negf * big + y + halfm;
+  const uint32_t ys = y + offs;
   const uint32_t q = __umulhi(ys, magic) >> 7;
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
@@ -96,7 +97,8 @@ __device__ __forceinline__ float residue_fast(int sx0, int sx1, int sx2, uint32_
 // Shifted path (0 < p <= kShiftMax for some element, e.g. k_A > 53): a' = u 2^p < 2^63 as
 // four 16-bit limbs, y = x3 c48 + x2 c32 + x1 c16 + x0 with |y| < 2^26, then the same single
 // Barrett step as the fast path: BIG = m 2^22 exceeds |y| when every modulus is above 16
-// (SplitConsts::shift_ok), and ys < 2^31 <= 2^39 / m keeps the quotient exact.
+// (SplitConsts::shift_ok), so ys = y + BIG + floor(m/2) > 0, and ys < 2^30 + 2^26 + m < 2^31
+// <= 2^39 / m keeps the quotient exact.
 constexpr uint32_t kShiftMax = 10;
 
 // Wide path (kShiftMax < p <= kWideMax for some element: k_A above 62, e.g. 17 or more
@@ -126,12 +128,12 @@ __device__ __forceinline__ float residue_wide(uint64_t packed, uint32_t m, const
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
 
-__device__ __forceinline__ float residue_shifted(int sx0, int sx1, int sx2, int sx3, uint32_t negf, uint32_t m,
-                                                 uint32_t c16, uint32_t c32, uint32_t c48, uint32_t magic,
-                                                 uint32_t big, uint32_t halfm, uint32_t fbase) {
+__device__ __forceinline__ float residue_shifted(int sx0, int sx1, int sx2, int sx3, uint32_t m, uint32_t c16,
+                                                 uint32_t c32, uint32_t c48, uint32_t magic, uint32_t offs,
+                                                 uint32_t fbase) {
   const uint32_t y = static_cast<uint32_t>(sx3 * static_cast<int>(c48) + sx2 * static_cast<int>(c32) +
                                            sx1 * static_cast<int>(c16) + sx0);
-  const uint32_t ys = negf * big + y + halfm;
+  const uint32_t ys = y + offs;
   const uint32_t q = __umulhi(ys, magic) >> 7;
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
@@ -161,7 +163,6 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
   if (warp_any_p && pmax <= kShiftMax && c.shift_ok) {
     // every a' of the warp is u 2^p with p <= kShiftMax: four signed 16-bit limbs of u 2^p
     int sx0[8], sx1[8], sx2[8], sx3[8];
-    uint32_t nf[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
       const uint64_t a = (v[x] & ((1ull << 53) - 1)) << pp[x];  // < 2^63
@@ -170,20 +171,19 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
       sx1[x] = sg * static_cast<int>(static_cast<uint32_t>(a) >> 16);
       sx2[x] = sg * static_cast<int>(static_cast<uint32_t>(a >> 32) & 0xFFFFu);
       sx3[x] = sg * static_cast<int>(static_cast<uint32_t>(a >> 48));
-      nf[x] = ng[x] ? 1u : 0u;
     }
 #pragma unroll 1
     for (int t = 0; t < c.s; ++t) {
       const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], c48 = c.c48[t],
                      mg = c.magic[t];
-      const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
+      const uint32_t halfm = m >> 1, offs = (m << 22) + halfm, fbase = 0x4B000080u - halfm;
       uint32_t w[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const float lo = residue_shifted(sx0[2 * x], sx1[2 * x], sx2[2 * x], sx3[2 * x], nf[2 * x], m, c16, c32,
-                                         c48, mg, big, halfm, fbase);
-        const float hi = residue_shifted(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], sx3[2 * x + 1],
-                                         nf[2 * x + 1], m, c16, c32, c48, mg, big, halfm, fbase);
+        const float lo = residue_shifted(sx0[2 * x], sx1[2 * x], sx2[2 * x], sx3[2 * x], m, c16, c32, c48, mg, offs,
+                                         fbase);
+        const float hi = residue_shifted(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], sx3[2 * x + 1], m, c16, c32,
+                                         c48, mg, offs, fbase);
         w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
       }
       if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -207,25 +207,22 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
   } else if (!warp_any_p) {
     // common case: every a' of the warp is u itself (no power-of-two factor)
     int sx0[8], sx1[8], sx2[8];
-    uint32_t nf[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
       const int sg = ng[x] ? -1 : 1;
       sx0[x] = sg * static_cast<int>(x0[x]);
       sx1[x] = sg * static_cast<int>(x1[x]);
       sx2[x] = sg * static_cast<int>(x2[x]);
-      nf[x] = ng[x] ? 1u : 0u;
     }
 #pragma unroll 1
     for (int t = 0; t < c.s; ++t) {
       const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-      const uint32_t big = m << 22, halfm = m >> 1, fbase = 0x4B000080u - halfm;
+      const uint32_t halfm = m >> 1, offs = (m << 22) + halfm, fbase = 0x4B000080u - halfm;
       uint32_t w[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        const float lo = residue_fast(sx0[2 * x], sx1[2 * x], sx2[2 * x], nf[2 * x], m, c16, c32, mg, big, halfm, fbase);
-        const float hi = residue_fast(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], nf[2 * x + 1], m, c16, c32, mg,
-                                      big, halfm, fbase);
+        const float lo = residue_fast(sx0[2 * x], sx1[2 * x], sx2[2 * x], m, c16, c32, mg, offs, fbase);
+        const float hi = residue_fast(sx0[2 * x + 1], sx1[2 * x + 1], sx2[2 * x + 1], m, c16, c32, mg, offs, fbase);
         w[x] = __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);  // two bf16
       }
       if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
