@@ -2,7 +2,7 @@
 //
 // [Ozaki II] Algorithm 1, steps 4-6.  Per output element, with residues
 // c_t = C''_t in [0, m_t) and P_t = M_t y_t (< M, so P_t / M = y_t / m_t):
-//   Z    = sum_t c_t P_t                      exact: 19/20-bit limb sums, then up to six 32-bit words
+//   Z    = sum_t c_t P_t                      exact: 16-bit limb sums (dot products), then up to six words
 //   Q    = round(Z / M) or one less            from the top limbs of Z in FP32
 //   X    = Z - Q M, then one correction by M  symmetric representative, |X| < M/2
 //   C    = RN(X 2^-(d_i + e_j))               one rounding, subnormals included
@@ -134,18 +134,20 @@ __device__ __forceinline__ bool round_normal_words(const uint32_t (&x)[kLimbs], 
 }
 
 // One thread = 4 consecutive rows i of one column j (a 4-byte load per modulus).
-// NL = 32-bit limbs needed for Z = sum_t c_t P_t (< 255 s M); the sum itself runs on
-// NS limbs of LB bits (P_t split the same way), each a 32-bit accumulator: every term
-// c_t P_t[l] is below 255 2^LB and s of them stay below 2^32, so the sums are exact
-// 32-bit multiply-adds (cheaper than 32 x 32 -> 64-bit ones); the limbs are then
-// carried into NL words.
-template <int NL, int LB, int NS>
+// NL = 32-bit words needed for Z = sum_t c_t P_t (< 255 s M).  The sum runs on N16
+// limbs of 16 bits of P_t, one 32-bit accumulator per limb, with two-way dot products
+// (dp2a: two 16-bit limbs of a pair of moduli times the pair's two residue bytes, plus
+// the accumulator): every term is below 255 2^16 and s of them stay below 2^32, so the
+// sums are exact, at one instruction per two moduli and limb.  The residues of four
+// moduli for one element come from a 4 x 4 byte transpose of the four elements' words.
+// The limbs are then carried into NL words.
+template <int NL, int N16>
 __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c, float inv_m_top,
                                                   const uint8_t* __restrict__ C_res,
                                                   const int32_t* __restrict__ rowexp,
                                                   const int32_t* __restrict__ colexp, double* __restrict__ C,
                                                   long long ldc) {
-  static_assert(LB >= 16 && LB <= 20 && NS <= kSmallLimbs && LB * (NS - 1) < 32 * NL, "CRT limb class");
+  static_assert(N16 >= 1 && N16 <= kHalfLimbs && N16 <= 2 * NL && kMaxModuli % 4 == 0, "CRT limb class");
   const int i0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (i0 >= m) return;
   const long long plane = static_cast<long long>(np) * mp;
@@ -161,21 +163,32 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
     for (int t = 0; t < kMaxModuli; ++t)
       res[t] = (t < c.s) ? __ldg(reinterpret_cast<const uint32_t*>(base + t * plane)) : 0u;
     double* out = C + i0 + j * ldc;
-    // Z = sum_t c_t P_t for the 4 elements at once, on LB-bit limbs (carries later):
-    // each constant limb is read once per 4 elements
-    uint32_t acc[4][NS];
+    // Z = sum_t c_t P_t for the 4 elements at once, on 16-bit limbs (carries later)
+    uint32_t acc[4][N16];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
 #pragma unroll
-      for (int l = 0; l < NS; ++l) acc[e][l] = 0;
+      for (int l = 0; l < N16; ++l) acc[e][l] = 0;
 #pragma unroll
-    for (int t = 0; t < kMaxModuli; ++t) {
-      if (t >= c.s) break;
+    for (int g = 0; g < kMaxModuli / 4; ++g) {
+      if (4 * g >= c.s) break;
+      // R[e] = residue bytes of moduli 4g .. 4g+3 for element e (res[t] holds modulus t
+      // for the 4 elements)
+      const uint32_t t0 = __byte_perm(res[4 * g], res[4 * g + 1], 0x5140u);
+      const uint32_t t1 = __byte_perm(res[4 * g], res[4 * g + 1], 0x7362u);
+      const uint32_t t2 = __byte_perm(res[4 * g + 2], res[4 * g + 3], 0x5140u);
+      const uint32_t t3 = __byte_perm(res[4 * g + 2], res[4 * g + 3], 0x7362u);
+      const uint32_t R[4] = {__byte_perm(t0, t2, 0x5410u), __byte_perm(t0, t2, 0x7632u),
+                             __byte_perm(t1, t3, 0x5410u), __byte_perm(t1, t3, 0x7632u)};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t r = __byte_perm(res[t], 0u, 0x4440u | static_cast<uint32_t>(e));  // byte e
+      for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int l = 0; l < NS; ++l) acc[e][l] += r * c.Ps[t][l];
+        for (int l = 0; l < N16; ++l) acc[e][l] = __dp2a_lo(c.Pd[2 * g][l], R[e], acc[e][l]);
+      if (4 * g + 2 < c.s) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+          for (int l = 0; l < N16; ++l) acc[e][l] = __dp2a_hi(c.Pd[2 * g + 1][l], R[e], acc[e][l]);
       }
     }
 #pragma unroll
@@ -189,18 +202,13 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         out[e] = 0.0;
         continue;
       }
-      // Z into NL words: word w collects the limbs that start in bits [32w, 32w + 32).
-      // Two limbs at most start in one word (LB >= 16), the lower one shifted by at most
-      // 31 - LB, so run < 2^63 + 2^44 + 2^32 never overflows.
+      // Z into NL words: word w holds limbs 2w and 2w + 1; run < 2^29 + 2^45 + 2^32.
       uint32_t x[kLimbs];
       uint64_t run = 0;
 #pragma unroll
       for (int w = 0; w < NL; ++w) {
-#pragma unroll
-        for (int l = 0; l < NS; ++l) {
-          const int pos = LB * l - 32 * w;
-          if (pos >= 0 && pos < 32) run += static_cast<uint64_t>(acc[e][l]) << pos;
-        }
+        if (2 * w < N16) run += acc[e][2 * w];
+        if (2 * w + 1 < N16) run += static_cast<uint64_t>(acc[e][2 * w + 1]) << 16;
         x[w] = static_cast<uint32_t>(run);
         run >>= 32;
       }
@@ -286,22 +294,22 @@ cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const u
   double Md = 0.0;
   for (int l = kLimbs - 1; l >= 0; --l) Md = Md * 4294967296.0 + c.M[l];
   const float inv_m_top = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / Md);
-  // (NL, LB, NS) classes: each s runs in the class of its NL and LB, with NS the class's
-  // largest limb count (unused top limbs of P_t are zero)
-#define OZ_CRT_LAUNCH(NLv, LBv, NSv) \
-  crt_kernel<NLv, LBv, NSv><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc)
-  if (nl == 3 && c.lb == 20 && c.ns <= 4)
-    OZ_CRT_LAUNCH(3, 20, 4);
-  else if (nl == 4 && c.lb == 20 && c.ns <= 6)
-    OZ_CRT_LAUNCH(4, 20, 6);
-  else if (nl == 5 && c.lb == 20 && c.ns <= 7)
-    OZ_CRT_LAUNCH(5, 20, 7);
-  else if (nl == 5 && c.lb == 19 && c.ns <= 8)
-    OZ_CRT_LAUNCH(5, 19, 8);
-  else if (nl == 6 && c.lb == 19 && c.ns <= 9)
-    OZ_CRT_LAUNCH(6, 19, 9);
-  else
-    return cudaErrorInvalidValue;  // no class for this moduli count (cannot happen for 2..20 moduli <= 256)
+  // (NL, N16) for each moduli count: the words of Z and the 16-bit limbs of M
+#define OZ_CRT_LAUNCH(NLv, N16v) \
+  crt_kernel<NLv, N16v><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc)
+  switch (nl * 16 + c.n16) {
+    case 3 * 16 + 1: OZ_CRT_LAUNCH(3, 1); break;
+    case 3 * 16 + 2: OZ_CRT_LAUNCH(3, 2); break;
+    case 3 * 16 + 3: OZ_CRT_LAUNCH(3, 3); break;
+    case 3 * 16 + 4: OZ_CRT_LAUNCH(3, 4); break;
+    case 3 * 16 + 5: OZ_CRT_LAUNCH(3, 5); break;
+    case 4 * 16 + 6: OZ_CRT_LAUNCH(4, 6); break;
+    case 4 * 16 + 7: OZ_CRT_LAUNCH(4, 7); break;
+    case 5 * 16 + 8: OZ_CRT_LAUNCH(5, 8); break;
+    case 5 * 16 + 9: OZ_CRT_LAUNCH(5, 9); break;
+    case 6 * 16 + 10: OZ_CRT_LAUNCH(6, 10); break;
+    default: return cudaErrorInvalidValue;  // no class for this moduli count (cannot happen for 2..20 moduli <= 256)
+  }
 #undef OZ_CRT_LAUNCH
   return cudaGetLastError();
 }

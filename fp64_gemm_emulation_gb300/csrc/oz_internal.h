@@ -11,7 +11,7 @@ namespace oz {
 
 constexpr int kMaxModuli = OZ_MAX_MODULI;
 constexpr int kLimbs = 6;        // 32-bit limbs for CRT values (M < 2^160 for 20 moduli)
-constexpr int kSmallLimbs = 9;   // 19- or 20-bit limbs of the CRT constants (9 x 19 >= 160 bits)
+constexpr int kHalfLimbs = 10;   // 16-bit limbs of the CRT constants (M < 2^160)
 constexpr int kPadM = 256;       // plane row padding (A rows, C_res rows)
 constexpr int kPadN = 256;       // plane row padding (B columns, C_res columns)
 constexpr int kPadK = 64;        // plane K padding (one 128-byte bf16 row of a stage)
@@ -38,9 +38,9 @@ struct CrtConsts {
   int kA;
   int mod[kMaxModuli];
   uint32_t P[kMaxModuli][kLimbs];  // M_t * y_t (< M), little-endian limbs
-  int lb;                          // bits per small limb: s 255 (2^lb - 1) < 2^32
-  int ns;                          // small limbs holding M (and every P_t < M)
-  uint32_t Ps[kMaxModuli][kSmallLimbs];  // P_t in lb-bit limbs, little-endian
+  int n16;                         // 16-bit limbs holding M (and every P_t < M)
+  // limb l of P_{2p} in the low half and of P_{2p+1} in the high half (zero past s)
+  uint32_t Pd[kMaxModuli / 2][kHalfLimbs];
   uint32_t frac[kMaxModuli];       // floor(2^32 * y_t / m_t): P_t / M in 0.32 fixed point
   uint32_t M[kLimbs];
   uint32_t halfM[kLimbs];          // floor(M / 2)

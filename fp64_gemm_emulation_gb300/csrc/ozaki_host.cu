@@ -177,22 +177,17 @@ int fill_crt_consts(int s, long long k_inner, CrtConsts* out) {
     out->M[l] = p.M.w[l];
     out->halfM[l] = half.w[l];
   }
-  // small limbs: the widest lb with s * 255 * (2^lb - 1) < 2^32 (20 up to 16 moduli, 19 up to 32)
-  out->lb = (static_cast<uint64_t>(s) * 255u * ((1u << 20) - 1u) < (1ull << 32)) ? 20 : 19;
   int mbits = 0;
   for (int l = kLimbs - 1; l >= 0 && !mbits; --l)
     if (p.M.w[l]) mbits = 32 * l + (32 - __builtin_clz(p.M.w[l]));
-  out->ns = (mbits + out->lb - 1) / out->lb;
-  if (out->ns > kSmallLimbs) return OZ_EINVAL;  // cannot happen for <= 20 moduli <= 256
+  out->n16 = (mbits + 15) / 16;
+  if (out->n16 > kHalfLimbs) return OZ_EINVAL;  // cannot happen for <= 20 moduli <= 256
   for (int t = 0; t < s; ++t) {
     out->mod[t] = p.mod[t];
     for (int l = 0; l < kLimbs; ++l) out->P[t][l] = p.P[t].w[l];
-    for (int l = 0; l < kSmallLimbs; ++l) {  // bits [lb l, lb l + lb) of P_t
-      const int pos = out->lb * l, w = pos >> 5, sh = pos & 31;
-      uint64_t win = 0;
-      if (w < kLimbs) win = p.P[t].w[w];
-      if (w + 1 < kLimbs) win |= static_cast<uint64_t>(p.P[t].w[w + 1]) << 32;
-      out->Ps[t][l] = static_cast<uint32_t>(win >> sh) & ((1u << out->lb) - 1u);
+    for (int l = 0; l < kHalfLimbs; ++l) {  // bits [16 l, 16 l + 16) of P_t
+      const uint32_t half = (p.P[t].w[l >> 1] >> (16 * (l & 1))) & 0xFFFFu;
+      out->Pd[t >> 1][l] |= half << (16 * (t & 1));
     }
     out->frac[t] = static_cast<uint32_t>((static_cast<uint64_t>(p.y[t]) << 32) / static_cast<uint64_t>(p.mod[t]));
   }
