@@ -14,6 +14,8 @@
 // All calls share the one buffer: calls whose work overlaps on the GPU (different
 // streams, or different host threads) race on it.  Nothing in it needs to start at
 // zero -- each step writes everything the next one reads.
+#include <atomic>
+
 #include "oz_internal.h"
 
 namespace oz {
@@ -22,22 +24,23 @@ namespace {
 static __device__ __align__(256) uint8_t g_noalloc_scratch[OZ_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<void*> g_scratch_addr[kMaxDevices] = {};  // several host threads may call at once
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array on the current device (looked up once per device;
+// concurrent first calls look up the same address).
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OZ_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return OZ_ENODEV;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
       return OZ_ECUDA;
     }
-    g_scratch_addr[dev] = p;
+    g_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return OZ_OK;
 }
 

@@ -5,6 +5,7 @@
 // coprime; the greedy descending list from 256 is used), M = prod m_t, M_t = M / m_t,
 // y_t = M_t^{-1} mod m_t (section 4), and k_A = k_B = the largest k with
 // q 2^(2k) <= M/2 - 1 (section 5), computed exactly on multi-limb integers.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -249,16 +250,17 @@ int cuda_rc(cudaError_t e) { return e == cudaSuccess ? OZ_OK : OZ_ECUDA; }
 // pool keeps the memory between calls instead of unmapping it at every
 // synchronisation (repeated calls then allocate in microseconds).
 void keep_default_pool_cached() {
-  static bool done[64] = {};
+  static std::atomic<bool> done[64] = {};  // several host threads may call at once
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || done[dev]) return;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || done[dev].load(std::memory_order_acquire))
+    return;
   cudaMemPool_t pool;
   if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
     uint64_t threshold = ~0ull;
-    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);  // idempotent
   }
   cudaGetLastError();
-  done[dev] = true;
+  done[dev].store(true, std::memory_order_release);
 }
 
 // A dimension cut into up to kMax blocks whose sizes are multiples of 256 (but the last).
