@@ -726,6 +726,7 @@ int ozaki1_dgemm_ex(int m, int n, int k, const double* A, int lda, const double*
   if (num_slices < 1 || num_slices > OZ_MAX_SLICES || !valid_variant(variant)) return OZ_EINVAL;
   if (m == 0 || n == 0) return OZ_OK;
   if (k == 0) return C ? (launch_fill_zero(m, n, C, ldc, stream) == cudaSuccess ? OZ_OK : OZ_ECUDA) : OZ_EINVAL;
+  if (!A || !B || !C) return OZ_EINVAL;  // argument errors before any allocation
   int beta;
   int rc = ozaki1_beta(k, &beta);
   if (rc) return rc;

@@ -565,6 +565,7 @@ int ozaki2_dgemm_ex(int m, int n, int k, const double* A, int lda, const double*
   if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI || !valid_scaling(scaling)) return OZ_EINVAL;
   if (m == 0 || n == 0) return OZ_OK;
   if (k == 0) return C ? cuda_rc(launch_fill_zero(m, n, C, ldc, stream)) : OZ_EINVAL;
+  if (!A || !B || !C) return OZ_EINVAL;  // argument errors before any allocation
   {
     int kA;
     if ((rc = ozaki2_scaling_k(num_moduli, k, scaling, &kA))) return rc;
@@ -589,6 +590,11 @@ int ozaki2_dgemm(int m, int n, int k, const double* A, int lda, const double* B,
   if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
   if (m == 0 || n == 0) return OZ_OK;
   if (k == 0) return C ? cuda_rc(launch_fill_zero(m, n, C, ldc, stream)) : OZ_EINVAL;
+  if (!A || !B || !C) return OZ_EINVAL;  // argument errors before any allocation
+  {
+    int kA;
+    if ((rc = ozaki2_choose_k(num_moduli, k, &kA))) return rc;
+  }
   const size_t bytes = ozaki2_workspace_bytes(m, n, k, num_moduli);
   keep_default_pool_cached();
   void* ws = nullptr;
@@ -779,14 +785,14 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
   return rc;
 }
 
-int ozaki_get_device_status(void) {
-  if (cudaDeviceSynchronize() != cudaSuccess) return OZ_ECUDA;
+int ozaki_get_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return OZ_ECUDA;
   int* p = device_status_ptr();
   if (!p) return OZ_ECUDA;
   int v = 0;
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return OZ_ECUDA;
-  const int zero = 0;
-  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return OZ_ECUDA;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemsetAsync(p, 0, sizeof(int), stream) != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess)
+    return OZ_ECUDA;
   return v;
 }
 

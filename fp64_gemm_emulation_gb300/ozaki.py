@@ -79,7 +79,7 @@ def _load():
         "ozaki1_accumulate_ex": (I, [I, I, I, I, I, P, P, P, P, I, P]),
         "ozaki1_dgemm_ex_ws": (I, [I, I, I, P, I, P, I, P, I, I, I, P, S, P]),
         "ozaki1_dgemm_ex": (I, [I, I, I, P, I, P, I, P, I, I, I, P]),
-        "ozaki_get_device_status": (I, []),
+        "ozaki_get_device_status": (I, [P]),
         "ozaki_status_string": (ctypes.c_char_p, [I]),
     }
     for name, (res, args) in sig.items():
@@ -512,8 +512,10 @@ def ozaki1_dgemm_ex_ws(A, B, num_slices: int, variant, workspace, C=None, stream
     return ozaki1_dgemm_ex(A, B, num_slices, variant, C=C, workspace=workspace, stream=stream)
 
 
-def ozaki_get_device_status() -> int:
-    return int(_lib.ozaki_get_device_status())
+def ozaki_get_device_status(stream=None) -> int:
+    """Status word of the current device after the work on ``stream`` (default: the current
+    torch stream) has finished; cleared by the read."""
+    return int(_lib.ozaki_get_device_status(_stream(stream)))
 
 
 def ozaki_status_string(code: int) -> str:

@@ -19,7 +19,7 @@
  *  - Return value: OZ_OK (0) or a negative oz_status.  Argument errors are reported
  *    synchronously before anything is launched.  A device-side failure (a bounded wait
  *    inside a kernel that expired) is recorded in a device status word that
- *    ozaki_get_device_status() returns.
+ *    ozaki_get_device_status(stream) returns.
  *  - m, n or k equal to 0: nothing is read; for k = 0 (m, n > 0) C is set to +0.0.
  *  - Inputs holding Inf or NaN: the affected rows of C (row of A) and columns of C
  *    (column of B) are set to NaN; nothing traps.
@@ -102,7 +102,8 @@ int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B,
 
 /* Steps a3+a4 (Algorithm 1 step 3): for every modulus t, the exact integer product
  * C'_t = A'_t B'_t on the tensor cores and C''_t = C'_t mod m_t, written to C_res.
- * Exact for every k (the k loop is folded mod m_t every 960 terms). */
+ * Exact for every k: each run of 1024 terms of the k loop is summed exactly on the
+ * tensor cores and folded mod m_t before the next starts. */
 int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_planes,
                         const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
 
@@ -305,19 +306,24 @@ int ozaki1_dgemm_ex(int m, int n, int k, const double* A, int lda, const double*
  * holds until the process exits.  Problems whose ozaki2_workspace_bytes(m, n, k,
  * num_moduli) exceeds it are rejected with OZ_ENOMEM before anything runs (at 14 moduli
  * m = n = k = 768 fits, 1024 does not).  The first call on each device looks up the
- * buffer's device address (with that device current); make that first call before any
- * stream capture.  All calls share the one buffer, which keeps the last call's
- * contents: calls that overlap on the GPU (other streams, other threads) race on it.
- * Same arguments, ordering and errors as ozaki2_dgemm otherwise. */
+ * buffer's device address (with that device current) and keeps it for that CUDA context;
+ * make that first call before any stream capture.  All calls share the one buffer, which
+ * keeps the last call's contents: calls that overlap on the GPU (other streams, other
+ * threads) race on it.  Arguments, ordering and errors are those of ozaki2_dgemm, checked
+ * in the same order (dimensions, moduli count, null pointers, OZ_ERANGE); the size limit
+ * (OZ_ENOMEM) is checked after them. */
 int ozaki2_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                          double* C, int ldc, int num_moduli, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- status */
 
-/* Synchronises the current device, returns the device status word (OZ_OK or
- * OZ_ETIMEOUT from a kernel's bounded wait) and clears it.  OZ_ECUDA if the
- * synchronisation itself fails. */
-int ozaki_get_device_status(void);
+/* Waits for the work queued on `stream` (0 = legacy default stream), then returns the
+ * device status word of the current device (OZ_OK, or OZ_ETIMEOUT if a kernel of this
+ * library gave up a bounded wait) and clears it.  The word is one per device: it holds
+ * what every kernel of this library on the device recorded up to the read, whatever
+ * stream launched it; a kernel still running on another stream may record later.  The
+ * read and the clear are ordered on `stream`.  OZ_ECUDA if a CUDA call fails. */
+int ozaki_get_device_status(cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* ozaki_status_string(int status);

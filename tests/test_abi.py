@@ -92,6 +92,24 @@ def test_argument_errors_are_synchronous(oz):
     assert oz.ozaki_status_string(oz.OZ_ETIMEOUT).startswith("OZ_ETIMEOUT")
 
 
+def test_noalloc_checks_arguments_in_the_order_of_ozaki2_dgemm(oz):
+    # every one of these returns before any CUDA call: null pointers and OZ_ERANGE come
+    # before the buffer's size limit, as in ozaki2_dgemm
+    lib = oz._lib
+    null = None
+    big = 4096  # its workspace is far beyond the fixed buffer
+    assert oz.ozaki2_workspace_bytes(big, big, big, 14) > oz.OZ_NOALLOC_SCRATCH_BYTES
+    assert lib.ozaki2_dgemm_noalloc(-1, 4, 4, null, 1, null, 4, null, 1, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_noalloc(8, 4, 4, null, 8, null, 4, null, 8, 21, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_noalloc(0, 4, 4, null, 1, null, 4, null, 1, 14, null) == oz.OZ_OK
+    assert lib.ozaki2_dgemm_noalloc(big, big, big, 1, big, 1, big, null, big, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_noalloc(big, big, big, null, big, 1, big, 1, big, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_noalloc(big, big, big, 1, big, null, big, 1, big, 14, null) == oz.OZ_EINVAL
+    assert lib.ozaki2_dgemm_noalloc(8, 8, 2**30, 1, 8, 1, 2**30, 1, 8, 2, null) == oz.OZ_ERANGE
+    assert lib.ozaki2_dgemm(8, 8, 2**30, 1, 8, 1, 2**30, 1, 8, 2, null) == oz.OZ_ERANGE
+    assert lib.ozaki2_dgemm_noalloc(big, big, big, 1, big, 1, big, 1, big, 14, null) == oz.OZ_ENOMEM
+
+
 def test_binding_names_follow_the_header(oz):
     for name in declared_functions():
         if name.startswith("ozaki"):
