@@ -29,6 +29,8 @@
 // OZ_ETIMEOUT in the device status word, drains what it issued and returns.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "oz_device.cuh"
 #include "oz_internal.h"
 
@@ -81,13 +83,26 @@ constexpr uint32_t kPaceDoneCredit = 1u << 24;
 constexpr uint64_t kPaceLimitNs = 100000;
 __device__ unsigned int g_pace_ctr[kPaceSlots];
 
+// The epilogue's accumulator-wait limit for the launches that follow (default 4 s).
+static std::atomic<unsigned long long> g_epi_wait_ns{kWaitLimitNs};
+unsigned long long epilogue_wait_ns() { return g_epi_wait_ns.load(std::memory_order_relaxed); }
+
 int* device_status_ptr() {
   int* p = nullptr;
   cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_status);
   return p;
 }
 
+// A wait expired: record it in the device status word and stop the pair (this CTA's abort
+// flag and the peer's, through its shared::cluster address).
 __device__ __forceinline__ void record_timeout(volatile int* abort_flag) {
+  *abort_flag = 1;
+  st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), cluster_ctarank() ^ 1u), 1u);
+  atomicExch(&g_status, OZ_ETIMEOUT);
+}
+
+// Same, for the teardown, which touches no shared memory of the peer.
+__device__ __forceinline__ void record_timeout_local(volatile int* abort_flag) {
   *abort_flag = 1;
   atomicExch(&g_status, OZ_ETIMEOUT);
 }
@@ -124,12 +139,20 @@ __device__ __forceinline__ void reduce_lanes(uint32_t (&run)[64], float m, float
 
 // Rendezvous of the epilogue warps on an mbarrier (one arrival per warp), with the same
 // bounded wait as every other wait in the kernel.  Returns false on expiry.
-__device__ __forceinline__ bool epilogue_sync(uint64_t* bar, uint32_t& phase) {
+// The warp's lanes agree on the outcome (a lane that saw the phase complete while another
+// gave up follows the one that gave up), so warp-wide instructions stay converged.
+__device__ __forceinline__ bool epilogue_sync(uint64_t* bar, uint32_t& phase, const volatile int* abort) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(bar, phase);
+  const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_or_abort(bar, phase, kWaitLimitNs, abort));
   phase ^= 1;
   return ok;
+}
+
+// The epilogue's wait for an accumulator, with the launch's limit, agreed by the warp.
+__device__ __forceinline__ bool epilogue_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              const volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_or_abort(bar, parity, limit_ns, abort));
 }
 
 struct UnitCoord {
@@ -225,8 +248,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   uint64_t* drain = accempty + 2;         // [1]       all MMAs of the pair done (both CTAs)
   uint64_t* epibar = drain + 1;           // [1]       epilogue warps rendezvous (per CTA)
   uint64_t* exitbar = epibar + 1;         // [1]       the peer has finished (per CTA)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(exitbar + 1);
+  uint64_t* proddone = exitbar + 1;       // [1]       both producers have stopped (used in the leader)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(proddone + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* issued_by = reinterpret_cast<volatile uint32_t*>(abort_flag + 1);  // [2] (leader)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();      // 0 = leader of the pair, 1 = peer
@@ -248,6 +273,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     mbar_init(drain, 1);
     mbar_init(epibar, EPI_WARPS);
     mbar_init(exitbar, 1);
+    mbar_init(proddone, 2);  // one arrival from each CTA's producer, after its last copy
     *abort_flag = 0;
     mbar_fence_init();
     tma_prefetch_desc(&tmA);
@@ -282,8 +308,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         const int rowB = uc.tn * BN + static_cast<int>(rank) * HALF_N;
         const int kb_end = min(nkb, (kblk + 1) * kbb);
         for (int kb = kblk * kbb; kb < kb_end; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            record_timeout(abort_flag);
+          if (*abort_flag) break;  // the pair has stopped: issue nothing more
+          if (!mbar_wait_or_abort(&empty[stage], phase ^ 1, kWaitLimitNs, abort_flag)) {
+            if (!*abort_flag) record_timeout(abort_flag);
             break;
           }
           const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
@@ -315,16 +342,24 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         }
       }
       if (pacer) atomicAdd(ctr, kPaceDoneCredit);  // finished: nobody waits for this pair
-      // Every issued copy must have landed before the pair may exit; the MMA thread has
-      // consumed them on the normal path.  The copies complete on the leader's barriers,
-      // which the leader's MMA thread drains (below); here wait for this CTA's stages to
-      // be released by the MMAs that read them.
-      for (int i = 0; i < kStages && i < issued; ++i) {
-        if (--stage < 0) {
-          stage = kStages - 1;
-          phase ^= 1;
+      // Every issued copy must have landed before the pair may exit.  The copies complete on
+      // the leader's barriers: tell the leader's MMA thread how many stages this CTA filled
+      // (it waits for any it did not consume, below), then, on the normal path, wait for
+      // this CTA's last stages to be released by the MMAs that read them.
+      st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(&issued_by[rank])), 0),
+                            static_cast<uint32_t>(issued));
+      mbar_arrive_release_cluster(mapa_shared(smem_u32(proddone), 0));
+      if (!*abort_flag) {
+        for (int i = 0; i < kStages && i < issued; ++i) {
+          if (--stage < 0) {
+            stage = kStages - 1;
+            phase ^= 1;
+          }
+          if (!mbar_wait_or_abort(&empty[stage], phase, kWaitLimitNs, abort_flag)) {
+            if (!*abort_flag) record_timeout(abort_flag);
+            break;
+          }
         }
-        if (!mbar_wait(&empty[stage], phase)) record_timeout(abort_flag);
       }
     }
   } else if (warp == 1) {
@@ -333,6 +368,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t g = 0;  // chunk counter: accumulator g & 1
+      uint32_t consumed = 0;  // stages whose copies this thread has waited for
       bool ok = true;
       for (int idx = 0; idx < sched.count() && ok && !*abort_flag; ++idx) {
         int u, kblk;
@@ -341,7 +377,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         const int nchunks = (kb_end - kb_begin + kbc - 1) / kbc;
         for (int ch = 0; ch < nchunks && ok; ++ch, ++g) {
           const uint32_t acc = g & 1;
-          if (!mbar_wait(&accempty[acc], ((g >> 1) & 1) ^ 1)) {
+          if (!mbar_wait_or_abort(&accempty[acc], ((g >> 1) & 1) ^ 1, kWaitLimitNs, abort_flag)) {
             ok = false;
             break;
           }
@@ -350,10 +386,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           const int kb0 = kb_begin + ch * kbc;
           const int kb1 = min(kb_end, kb0 + kbc);
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase)) {
+            if (!mbar_wait_or_abort(&full[stage], phase, kWaitLimitNs, abort_flag)) {
               ok = false;
               break;
             }
+            ++consumed;
             tc_fence_after();
             const uint32_t a_addr = smem_u32(sA + stage * A_STAGE);
             const uint32_t b_addr = smem_u32(sB + stage * B_STAGE);
@@ -376,7 +413,27 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           umma_commit_pair(&accfull[acc], 0x3);  // the chunk is in both CTAs' TMEM
         }
       }
-      if (!ok) record_timeout(abort_flag);
+      if (!ok && !*abort_flag) record_timeout(abort_flag);
+      // Account for every copy before the pair may exit: once both producers have stopped
+      // (and published how many stages they filled), wait for each stage filled after the
+      // last one consumed here, arriving for a producer that stopped before filling it, so
+      // that its phase completes exactly when the copies that were issued have landed.
+      // (On the normal path both producers filled exactly the stages consumed here.)
+      if (mbar_wait_acquire_cluster(proddone, 0)) {
+        const uint32_t n0 = issued_by[0], n1 = issued_by[1];
+        const uint32_t top = n0 > n1 ? n0 : n1;
+        for (uint32_t q = consumed; q < top && q < consumed + kStages; ++q) {  // at most kStages are in flight
+          const int st = static_cast<int>(q % kStages);
+          if (q >= n0) mbar_arrive(&full[st]);
+          if (q >= n1) mbar_arrive(&full[st]);
+          if (!mbar_wait(&full[st], (q / kStages) & 1)) {
+            record_timeout(abort_flag);
+            break;
+          }
+        }
+      } else {
+        record_timeout(abort_flag);
+      }
       umma_commit_pair(drain, 0x3);  // arrives in both CTAs once every MMA above is done
     }
   } else {
@@ -402,9 +459,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         sched.at(idx, u, kblk);
         const UnitCoord uc = unit_coord(u, tiles_m, tiles_n);
         const uint32_t acc = g & 1;
-        if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+        if (!epilogue_wait(&accfull[acc], (g >> 1) & 1, c.epi_wait_ns, abort_flag)) {
           ok = false;
-          if (lane == 0) record_timeout(abort_flag);
+          if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
           break;
         }
         tc_fence_after();
@@ -448,9 +505,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         int32_t run[64];
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
-          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+          if (!epilogue_wait(&accfull[acc], (g >> 1) & 1, c.epi_wait_ns, abort_flag)) {
             ok = false;
-            if (lane == 0) record_timeout(abort_flag);
+            if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
             break;
           }
           tc_fence_after();
@@ -497,9 +554,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             outp + uc.t * plane + static_cast<long long>(uc.tn * BN + half * 128) * mp + uc.tm * BM + row_off + row;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
-          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+          if (!epilogue_wait(&accfull[acc], (g >> 1) & 1, c.epi_wait_ns, abort_flag)) {
             ok = false;
-            if (lane == 0) record_timeout(abort_flag);
+            if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
             break;
           }
           tc_fence_after();
@@ -544,9 +601,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         for (int i = 0; i < 64; ++i) run[i] = 0;
         for (int ch = 0; ch < nchunks; ++ch, ++g) {
           const uint32_t acc = g & 1;
-          if (!mbar_wait(&accfull[acc], (g >> 1) & 1)) {
+          if (!epilogue_wait(&accfull[acc], (g >> 1) & 1, c.epi_wait_ns, abort_flag)) {
             ok = false;
-            if (lane == 0) record_timeout(abort_flag);
+            if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
             break;
           }
           tc_fence_after();
@@ -585,8 +642,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             *reinterpret_cast<uint4*>(stash + col * HALF_M + part * 16) =
                 *reinterpret_cast<const uint4*>(dst + static_cast<long long>(col) * mp + part * 16);
           }
-          if (!epilogue_sync(epibar, eph)) {
-            if (lane == 0) record_timeout(abort_flag);
+          if (!epilogue_sync(epibar, eph, abort_flag)) {
+            if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
             break;
           }
         }
@@ -603,8 +660,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           col0[(2 * i) * HALF_M] = static_cast<uint8_t>(lo);
           col0[(2 * i + 1) * HALF_M] = static_cast<uint8_t>(hi);
         }
-        if (!epilogue_sync(epibar, eph)) {
-          if (lane == 0) record_timeout(abort_flag);
+        if (!epilogue_sync(epibar, eph, abort_flag)) {
+          if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
           break;
         }
 
@@ -615,8 +672,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
           *reinterpret_cast<uint4*>(dst + static_cast<long long>(col) * mp + part * 16) =
               *reinterpret_cast<const uint4*>(stash + col * HALF_M + part * 16);
         }
-        if (!epilogue_sync(epibar, eph)) {
-          if (lane == 0) record_timeout(abort_flag);
+        if (!epilogue_sync(epibar, eph, abort_flag)) {
+          if (lane == 0 && !*abort_flag) record_timeout(abort_flag);
           break;
         }
       }
@@ -628,10 +685,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     // every MMA of the pair (and every commit before it) has completed ...
-    if (!mbar_wait(drain, 0)) record_timeout(abort_flag);
+    if (!mbar_wait(drain, 0)) record_timeout_local(abort_flag);
     // ... and the peer is done with this CTA's barriers and shared memory
     mbar_arrive_cluster(mapa_shared(smem_u32(exitbar), rank ^ 1u));
-    if (!mbar_wait(exitbar, 0)) record_timeout(abort_flag);
+    if (!mbar_wait(exitbar, 0)) record_timeout_local(abort_flag);
   }
   __syncthreads();
   tc_fence_after();
@@ -712,6 +769,7 @@ static int launch_gemm(int mp, int np, int kp, int a_planes, int b_planes, const
   const int nkb = kp / BK;
   GemmConsts cl = c;
   cl.launch_id = next_launch_id();
+  cl.epi_wait_ns = epilogue_wait_ns();
   {  // zero this launch's pacing counter on the stream
     unsigned int* ctr = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ctr), g_pace_ctr) != cudaSuccess) return OZ_ECUDA;
@@ -754,3 +812,10 @@ int launch_bound_gemm(int mp, int np, int kp, const uint16_t* A_plane, const uin
 }
 
 }  // namespace oz
+
+extern "C" int ozaki_set_epilogue_wait_ns(long long ns) {
+  if (ns < -1) return OZ_EINVAL;
+  oz::g_epi_wait_ns.store(ns == -1 ? oz::kWaitLimitNs : static_cast<unsigned long long>(ns),
+                          std::memory_order_relaxed);
+  return OZ_OK;
+}

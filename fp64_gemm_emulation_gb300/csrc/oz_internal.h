@@ -41,7 +41,6 @@ struct CrtConsts {
   int n16;                         // 16-bit limbs holding M (and every P_t < M)
   // limb l of P_{2p} in the low half and of P_{2p+1} in the high half (zero past s)
   uint32_t Pd[kMaxModuli / 2][kHalfLimbs];
-  uint32_t frac[kMaxModuli];       // floor(2^32 * y_t / m_t): P_t / M in 0.32 fixed point
   uint32_t M[kLimbs];
   uint32_t halfM[kLimbs];          // floor(M / 2)
 };
@@ -60,6 +59,7 @@ struct GemmConsts {
   int kb_per_block;   // k-blocks of 64 per scheduling K-block (a multiple of kb_per_chunk)
   uint32_t launch_id; // selects this launch's pacing counter
   int grouped;        // accumulation only: the number of batches in prod_first (0: none)
+  unsigned long long epi_wait_ns;  // time limit of the epilogue's wait for an accumulator
   float modf[kMaxModuli];
   float invf[kMaxModuli];
   uint8_t a_plane[kMaxPairs];
@@ -100,5 +100,9 @@ cudaError_t launch_fill_zero(int m, int n, double* C, int ldc, cudaStream_t stre
 
 // Device status word (set by kernels whose bounded waits expired).
 int* device_status_ptr();
+
+// Time limit of the GEMM epilogue's accumulator wait for the launches that follow
+// (ozaki_set_epilogue_wait_ns).
+unsigned long long epilogue_wait_ns();
 
 }  // namespace oz

@@ -190,7 +190,6 @@ int fill_crt_consts(int s, long long k_inner, CrtConsts* out) {
       const uint32_t half = (p.P[t].w[l >> 1] >> (16 * (l & 1))) & 0xFFFFu;
       out->Pd[t >> 1][l] |= half << (16 * (t & 1));
     }
-    out->frac[t] = static_cast<uint32_t>((static_cast<uint64_t>(p.y[t]) << 32) / static_cast<uint64_t>(p.mod[t]));
   }
   return OZ_OK;
 }

@@ -81,6 +81,7 @@ def _load():
         "ozaki1_dgemm_ex": (I, [I, I, I, P, I, P, I, P, I, I, I, P]),
         "ozaki_get_device_status": (I, [P]),
         "ozaki_status_string": (ctypes.c_char_p, [I]),
+        "ozaki_set_epilogue_wait_ns": (I, [L]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -516,6 +517,11 @@ def ozaki_get_device_status(stream=None) -> int:
     """Status word of the current device after the work on ``stream`` (default: the current
     torch stream) has finished; cleared by the read."""
     return int(_lib.ozaki_get_device_status(_stream(stream)))
+
+
+def ozaki_set_epilogue_wait_ns(ns: int) -> None:
+    """Time limit of the GEMM epilogue's accumulator wait for later launches (-1: default 4 s)."""
+    _check(_lib.ozaki_set_epilogue_wait_ns(int(ns)), "ozaki_set_epilogue_wait_ns")
 
 
 def ozaki_status_string(code: int) -> str:

@@ -325,6 +325,16 @@ int ozaki2_dgemm_noalloc(int m, int n, int k, const double* A, int lda, const do
  * read and the clear are ordered on `stream`.  OZ_ECUDA if a CUDA call fails. */
 int ozaki_get_device_status(cudaStream_t stream);
 
+/* Time limit, in nanoseconds, of one wait inside the tensor-core GEMM kernels launched
+ * after this call: the epilogue's wait for an accumulator of exact sums.  -1 restores the
+ * default of 4 s; 0 makes the wait give up as soon as it finds the accumulator not ready,
+ * so that a test can drive the failure path on purpose.  On expiry the kernel records
+ * OZ_ETIMEOUT in the device status word, stops both CTAs of the pair, waits for every copy
+ * and MMA it issued, frees its tensor memory and returns; its outputs are then undefined.
+ * A process-wide setting.  The pages have no counterpart: this is a library facility for
+ * exercising failure detection.  OZ_EINVAL for ns < -1. */
+int ozaki_set_epilogue_wait_ns(long long ns);
+
 /* Human-readable name of a status code (static string). */
 const char* ozaki_status_string(int status);
 

@@ -223,3 +223,10 @@ def test_ozaki1_variant_workspace_and_errors(oz):
     assert lib.ozaki1_dgemm_ex(8, 4, 4, 1, 8, 1, 4, 1, 8, 7, 3, null) == oz.OZ_EINVAL
     assert lib.ozaki1_dgemm_ex_ws(8, 8, 8, 1, 8, 1, 8, 1, 8, 7, 1, 256, 16, null) == oz.OZ_ENOMEM
     assert lib.ozaki1_num_batches(0, 16, 1, ctypes.byref(ctypes.c_int())) == oz.OZ_EINVAL
+
+
+def test_epilogue_wait_setting_checks_its_argument(oz):
+    lib = oz._lib
+    assert lib.ozaki_set_epilogue_wait_ns(-2) == oz.OZ_EINVAL
+    assert lib.ozaki_set_epilogue_wait_ns(1000) == oz.OZ_OK
+    assert lib.ozaki_set_epilogue_wait_ns(-1) == oz.OZ_OK  # back to the default
