@@ -252,6 +252,92 @@ def cpu_baseline_measure():
     return out
 
 
+# ------------------------------------------------------------------ CPU-oracle timing protocol
+# The oracle on the host cores, as a stated baseline (never a target): complete runs where
+# it finishes (256^3 and 4096^3), and at the larger configurations the exponents and the
+# residue planes of both operands in full (O(N^2) work) plus the exact products, CRT and
+# rounding on 64 seeded 64 x 64 output tiles, extrapolated linearly by the tile fraction.
+ORACLE_FULL = [(256, 256, 256, 14, 0.5), (4096, 4096, 4096, 14, 0.5)]
+ORACLE_SAMPLED = [(8192, 8192, 8192, 14, 1.0), (16384, 16384, 16384, 14, 0.5), (2048, 2048, 262144, 14, 0.5)]
+
+
+def _oracle_full(m, n, k, s, phi):
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+    from oracle import ozaki2 as O
+
+    A, B = hpl_like(m, n, k, phi=phi, seed=SEED)
+    t0 = time.perf_counter()
+    O.ozaki2_dgemm(A, B, s, keep=False)
+    return time.perf_counter() - t0
+
+
+def _plane_block(args):
+    from oracle import ozaki2 as O
+
+    X, dd, moduli = args
+    return O.residue_planes(O.scaled_trunc_matrix(X, dd), moduli)
+
+
+def _oracle_sampled(m, n, k, s, phi, workers, tiles=64, tile=64):
+    import multiprocessing as mp
+
+    from fp64_gemm_emulation_gb300.inputs import hpl_like
+    from oracle import ozaki2 as O
+
+    A, B = hpl_like(m, n, k, phi=phi, seed=SEED)
+    Bt = B.T
+    with mp.get_context("spawn").Pool(workers) as pool:
+        t0 = time.perf_counter()
+        cc = O.crt_constants(O.greedy_moduli(s))
+        kA = O.choose_k(cc.M, k)
+        EA, EB = O.row_exponents(A), O.row_exponents(Bt)
+        d, e = O.scale_exponents(EA, kA), O.scale_exponents(EB, kA)
+        blk = max(1, min((1 << 22) // k, -(-max(m, n) // (4 * workers))))  # <= 4 Mi elements, >= 4 blocks a process
+        Ares = np.empty((s, m, k), dtype=np.int8)
+        Bres = np.empty((s, n, k), dtype=np.int8)
+        for X, dd, P, rows in ((A, d, Ares, m), (Bt, e, Bres, n)):
+            starts = list(range(0, rows, blk))
+            jobs = ((np.ascontiguousarray(X[r0:r0 + blk]), dd[r0:r0 + blk], cc.moduli) for r0 in starts)
+            for r0, planes in zip(starts, pool.imap(_plane_block, jobs)):
+                P[:, r0:r0 + planes.shape[1]] = planes
+        t_planes = time.perf_counter() - t0
+    rng = np.random.default_rng(SEED)
+    t1 = time.perf_counter()
+    for _ in range(tiles):
+        i0 = int(rng.integers(0, m // tile)) * tile
+        j0 = int(rng.integers(0, n // tile)) * tile
+        Cres = O.residue_products(Ares[:, i0:i0 + tile], np.transpose(Bres[:, j0:j0 + tile], (0, 2, 1)), cc.moduli)
+        O.unscale(O.crt_reconstruct(Cres, cc), d[i0:i0 + tile], e[j0:j0 + tile])
+    t_tiles = time.perf_counter() - t1
+    return t_planes, t_tiles, t_planes + t_tiles * (m * n) / (tiles * tile * tile)
+
+
+def oracle_protocol_entry(kind, m, n, k, s, phi, workers=1):
+    if kind == "full":
+        dt = _oracle_full(m, n, k, s, phi)
+        return {"workload": f"{m}x{n}x{k} s={s} phi={phi}", "seconds": dt, "measured": "complete run",
+                "tflops": 2.0 * m * n * k / dt / 1e12}
+    t_planes, t_tiles, total = _oracle_sampled(m, n, k, s, phi, workers)
+    return {"workload": f"{m}x{n}x{k} s={s} phi={phi}", "seconds": total,
+            "measured": f"extrapolated: exponents + residue planes in full ({workers} processes) {t_planes:.1f} s, "
+                        f"products + CRT + rounding on 64 seeded 64x64 tiles {t_tiles:.1f} s, "
+                        f"scaled by the tile fraction",
+            "tflops": 2.0 * m * n * k / total / 1e12}
+
+
+def run_oracle_protocol(one_core: bool):
+    """One JSON line per configuration.  All host cores: BLAS threads for the products and
+    one process per core for the element-wise plane work of the sampled configurations.
+    One core: one BLAS thread, the complete runs only."""
+    cores = 1 if one_core else os.cpu_count()
+    plan = [("full", c) for c in ORACLE_FULL] + ([] if one_core else [("sampled", c) for c in ORACLE_SAMPLED])
+    for kind, (m, n, k, s, phi) in plan:
+        out = oracle_protocol_entry(kind, m, n, k, s, phi, workers=cores)
+        out.update({"kind": "oracle", "cores": cores, "unit": UNIT})
+        print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -519,7 +605,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true")
     ap.add_argument("--no-variants", action="store_true")
+    ap.add_argument("--oracle-protocol", action="store_true",
+                    help="time the CPU oracle at the workload configurations (full or sampled) and exit")
+    ap.add_argument("--one-core", action="store_true", help="with --oracle-protocol: one BLAS thread")
     args = ap.parse_args()
+    if args.oracle_protocol:
+        if args.one_core:
+            for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+                if os.environ.get(v) != "1":  # the BLAS reads these when numpy loads: start afresh
+                    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+                    return subprocess.run([sys.executable] + sys.argv, env=env).returncode
+        return run_oracle_protocol(args.one_core)
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
