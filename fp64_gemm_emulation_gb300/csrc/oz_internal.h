@@ -80,6 +80,9 @@ cudaError_t launch_floor_exponents(int m, int n, int k, const double* A, int lda
 cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,
                          const int32_t* exps, const SplitConsts& c, uint16_t* planes, int rows_padded,
                          int kp, cudaStream_t stream);
+cudaError_t launch_split_fused_kcontig(int rows, int k, const double* X, long long ld, const SplitConsts& c,
+                                       int32_t* exps, uint16_t* planes, int rows_padded, int kp,
+                                       cudaStream_t stream);
 int launch_residue_gemm(int mp, int np, int kp, const GemmConsts& c, const uint16_t* A_planes,
                         const uint16_t* B_planes, uint8_t* C_res, cudaStream_t stream);
 int launch_slice_gemm(int mp, int np, int kp, int a_planes, int b_planes, const GemmConsts& c,

@@ -11,6 +11,7 @@
 // packed (sign, p, u) words in shared memory; phase 2 reads them along k and writes
 // 16-byte vectors of 8 bf16 residues per modulus, so the K-contiguous planes are
 // written in full 128-byte rows.
+#include "oz_fp.cuh"
 #include "oz_internal.h"
 
 namespace oz {
@@ -311,6 +312,55 @@ __global__ void __launch_bounds__(256, 4) split_kcontig_kernel(int rows, int K, 
   }
   residues_to_planes(v, c, valid ? planes + static_cast<long long>(r) * kp + k0 : nullptr,
                      static_cast<long long>(rows_padded) * kp);
+}
+
+// Steps a1 + a2 for a K-contiguous operand (B: column j is k contiguous) with one DRAM read
+// of each column: one block per row of the operand (a column of B) takes the row's largest
+// magnitude (the same integer maximum of the 63-bit patterns as the exponent kernels),
+// writes F_j = ceil(log2 max), then splits the row, whose second read comes from L2 (a few
+// blocks per SM keep about 40 MB of rows in flight, well inside the 129 MB L2).  Padding rows
+// (r >= rows) write zero planes.
+constexpr int kFusedThreads = 256;
+
+__global__ void __launch_bounds__(kFusedThreads, 3)
+    split_kcontig_fused_kernel(int rows, int K, const double* __restrict__ X, long long ld, const SplitConsts c,
+                               int32_t* __restrict__ exps, uint16_t* __restrict__ planes, int rows_padded, int kp) {
+  __shared__ unsigned long long warp_max[kFusedThreads / 32];
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int groups = kp >> 3;
+  const double* src = X + static_cast<long long>(r) * ld;
+  unsigned long long mag = 0;
+  if (r < rows) {
+#pragma unroll 8
+    for (int kk = tid; kk < K; kk += kFusedThreads) mag = max(mag, magnitude_bits(__ldg(src + kk)));
+  }
+#pragma unroll
+  for (int off = 16; off; off >>= 1) mag = max(mag, __shfl_xor_sync(0xFFFFFFFFu, mag, off));
+  if (lane == 0) warp_max[warp] = mag;
+  __syncthreads();
+  mag = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < kFusedThreads / 32; ++w) mag = max(mag, warp_max[w]);
+  const int E = mag ? ceil_log2_code(__longlong_as_double(static_cast<long long>(mag))) : OZ_EXP_EMPTY;
+  if (tid == 0 && r < rows) exps[r] = E;
+  const long long plane_elems = static_cast<long long>(rows_padded) * kp;
+  for (int g0 = 0; g0 < groups; g0 += kFusedThreads) {  // block-uniform trip count
+    const int g = g0 + tid;
+    const int k0 = 8 * g;
+    uint64_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (r < rows && g < groups && k0 + e < K) ? pack_scaled(__ldg(src + k0 + e), E, c.kA) : 0ull;
+    residues_to_planes(v, c, g < groups ? planes + static_cast<long long>(r) * kp + k0 : nullptr, plane_elems);
+  }
+}
+
+cudaError_t launch_split_fused_kcontig(int rows, int k, const double* X, long long ld, const SplitConsts& c,
+                                       int32_t* exps, uint16_t* planes, int rows_padded, int kp,
+                                       cudaStream_t stream) {
+  split_kcontig_fused_kernel<<<rows_padded, kFusedThreads, 0, stream>>>(rows, k, X, ld, c, exps, planes, rows_padded,
+                                                                        kp);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_split(int rows, int k, const double* X, long long row_stride, long long k_stride,

@@ -464,6 +464,29 @@ int ozaki2_split_ex(int m, int n, int k, const double* A, int lda, const double*
   return OZ_OK;
 }
 
+int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
+                       int32_t* rowexp, int32_t* colexp, uint16_t* A_planes, uint16_t* B_planes,
+                       cudaStream_t stream) {
+  if (m < 0 || n < 0 || k < 1) return OZ_EINVAL;
+  if ((A && (lda < (m > 1 ? m : 1) || !rowexp || !A_planes)) || (B && (ldb < (k > 1 ? k : 1) || !colexp || !B_planes)))
+    return OZ_EINVAL;
+  if (num_moduli < OZ_MIN_MODULI || num_moduli > OZ_MAX_MODULI) return OZ_EINVAL;
+  SplitConsts sc;
+  int rc = fill_split_consts(num_moduli, k, &sc);
+  if (rc) return rc;
+  if (A && m > 0) {
+    if ((rc = ozaki2_exponents(m, 0, k, A, lda, nullptr, 1, rowexp, nullptr, stream))) return rc;
+    if ((rc = ozaki2_split(m, 0, k, A, lda, nullptr, 1, num_moduli, rowexp, nullptr, A_planes, nullptr, stream)))
+      return rc;
+  }
+  if (B && n > 0) {
+    const int np = static_cast<int>(roundup(n, kPadN)), kp = static_cast<int>(roundup(k, kPadK));
+    // each column of B from DRAM once: its maximum, then its residues (second read from L2)
+    return cuda_rc(launch_split_fused_kcontig(n, k, B, ldb, sc, colexp, B_planes, np, kp, stream));
+  }
+  return OZ_OK;
+}
+
 int ozaki2_residue_gemm(int m, int n, int k, int num_moduli, const uint16_t* A_planes, const uint16_t* B_planes,
                         uint8_t* C_res, cudaStream_t stream) {
   if (m < 0 || n < 0 || k < 1 || !A_planes || !B_planes || !C_res) return OZ_EINVAL;
@@ -515,8 +538,7 @@ int ozaki2_dgemm_ws(int m, int n, int k, const double* A, int lda, const double*
   uint16_t* Ap = reinterpret_cast<uint16_t*>(ws + L.off_A);
   uint16_t* Bp = reinterpret_cast<uint16_t*>(ws + L.off_B);
   uint8_t* Cr = ws + L.off_C;
-  if ((rc = ozaki2_exponents(m, n, k, A, lda, B, ldb, rowexp, colexp, stream))) return rc;
-  if ((rc = ozaki2_split(m, n, k, A, lda, B, ldb, num_moduli, rowexp, colexp, Ap, Bp, stream))) return rc;
+  if ((rc = ozaki2_scale_split(m, n, k, A, lda, B, ldb, num_moduli, rowexp, colexp, Ap, Bp, stream))) return rc;
   if ((rc = ozaki2_residue_gemm(m, n, k, num_moduli, Ap, Bp, Cr, stream))) return rc;
   return ozaki2_crt(m, n, k, num_moduli, Cr, rowexp, colexp, C, ldc, stream);
 }
@@ -747,8 +769,7 @@ int ozaki2_dgemm_host(int m, int n, int k, const double* A, int lda, const doubl
     }
     if (!splitB[j]) {
       if (!rc && cudaStreamWaitEvent(scomp, evB[j], 0) != cudaSuccess) rc = OZ_ECUDA;
-      if (!rc) rc = ozaki2_exponents(0, nj, k, nullptr, 1, dBj, k, nullptr, colexp + j0, scomp);
-      if (!rc) rc = ozaki2_split(0, nj, k, nullptr, 1, dBj, k, s, nullptr, colexp + j0, nullptr, Bp, scomp);
+      if (!rc) rc = ozaki2_scale_split(0, nj, k, nullptr, 1, dBj, k, s, nullptr, colexp + j0, nullptr, Bp, scomp);
       splitB[j] = true;
     }
     if (!rc) rc = ozaki2_residue_gemm(mi, nj, k, s, Ap, Bp, Cr, scomp);

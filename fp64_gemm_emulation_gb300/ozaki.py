@@ -49,6 +49,7 @@ def _load():
         "ozaki2_exponents": (I, [I, I, I, P, I, P, I, P, P, P]),
         "ozaki2_split": (I, [I, I, I, P, I, P, I, I, P, P, P, P, P]),
         "ozaki2_residue_gemm": (I, [I, I, I, I, P, P, P, P]),
+        "ozaki2_scale_split": (I, [I, I, I, P, I, P, I, I, P, P, P, P, P]),
         "ozaki2_crt": (I, [I, I, I, I, P, P, P, P, I, P]),
         "ozaki2_dgemm_ws": (I, [I, I, I, P, I, P, I, P, I, I, P, S, P]),
         "ozaki2_dgemm": (I, [I, I, I, P, I, P, I, P, I, I, P]),
@@ -169,6 +170,25 @@ def ozaki2_split(A, B, num_moduli: int, rowexp, colexp, stream=None):
     _check(_lib.ozaki2_split(m, n, k, _ptr(A), _ld(A), _ptr(B), _ld(B), num_moduli, _ptr(rowexp), _ptr(colexp),
                              _ptr(Ap), _ptr(Bp), _stream(stream)), "ozaki2_split")
     return Ap, Bp
+
+
+def ozaki2_scale_split(A, B, num_moduli: int, stream=None):
+    """Steps a1 + a2 in one call: (rowexp, colexp, A_planes, B_planes); either operand may be None."""
+    import torch
+
+    dev = (A if A is not None else B).device
+    k = A.shape[1] if A is not None else B.shape[0]
+    m = A.shape[0] if A is not None else 0
+    n = B.shape[1] if B is not None else 0
+    mp, np_, kp = ozaki2_plane_dims(m, n, k)
+    rowexp = torch.empty(m, dtype=torch.int32, device=dev) if A is not None else None
+    colexp = torch.empty(n, dtype=torch.int32, device=dev) if B is not None else None
+    Ap = torch.empty((num_moduli, mp, kp), dtype=torch.int16, device=dev) if A is not None else None
+    Bp = torch.empty((num_moduli, np_, kp), dtype=torch.int16, device=dev) if B is not None else None
+    _check(_lib.ozaki2_scale_split(m, n, k, _ptr(A), _ld(A) if A is not None else 1, _ptr(B),
+                                   _ld(B) if B is not None else 1, num_moduli, _ptr(rowexp), _ptr(colexp),
+                                   _ptr(Ap), _ptr(Bp), _stream(stream)), "ozaki2_scale_split")
+    return rowexp, colexp, Ap, Bp
 
 
 def ozaki2_residue_gemm(m: int, n: int, k: int, num_moduli: int, A_planes, B_planes, stream=None):

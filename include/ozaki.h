@@ -100,6 +100,15 @@ int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B,
                  int num_moduli, const int32_t* rowexp, const int32_t* colexp,
                  uint16_t* A_planes, uint16_t* B_planes, cudaStream_t stream);
 
+/* Steps a1 and a2 together (Algorithm 1 steps 2-3, left half): the exponents of
+ * ozaki2_exponents and the planes of ozaki2_split, same arguments, layouts and errors, in
+ * fewer passes over DRAM: each column of B is read from DRAM once (its maximum, then its
+ * residues, the second read served by L2); A takes the two passes.  Either operand may be
+ * skipped with NULL for its source, exponents and planes. */
+int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
+                       int num_moduli, int32_t* rowexp, int32_t* colexp, uint16_t* A_planes,
+                       uint16_t* B_planes, cudaStream_t stream);
+
 /* Steps a3+a4 (Algorithm 1 step 3): for every modulus t, the exact integer product
  * C'_t = A'_t B'_t on the tensor cores and C''_t = C'_t mod m_t, written to C_res.
  * Exact for every k: each run of 1024 terms of the k loop is summed exactly on the

@@ -91,6 +91,11 @@ def test_steps_bit_exact(oz, m, n, k, s, phi, seed):
     assert not Ai[:, m:, :].any() and not Ai[:, :, k:].any()      # zero padding
     assert not Bi[:, n:, :].any() and not Bi[:, :, k:].any()
 
+    # steps a1 + a2 in one call (one pass over each column of B): the same bits
+    re2, ce2, Ap2, Bp2 = oz.ozaki2_scale_split(dA, dB, s)
+    assert torch.equal(re2, rowexp) and torch.equal(ce2, colexp)
+    assert torch.equal(Ap2, Ap) and torch.equal(Bp2, Bp)
+
     Cr = oz.ozaki2_residue_gemm(m, n, k, s, Ap, Bp)
     got = Cr.cpu().numpy()[:, :n, :m]                               # [s][j][i]
     assert np.array_equal(got, np.transpose(ref.Cres, (0, 2, 1)).astype(np.uint8))
@@ -337,3 +342,30 @@ def test_split_with_large_shifts(oz, s, k):
     assert np.array_equal(bf16_planes_to_int(Bp)[:, :n, :k], np.transpose(ref.Bres, (0, 2, 1)).astype(np.int64))
     C = oz.ozaki2_dgemm(dA, dB, s)
     assert np.array_equal(bits(host(C)), bits(ref.C))
+
+
+# the one-pass split of B holds 8, 16 or 32 values a thread (Kp up to 4096, 8192, 16384); above
+# that the two-pass path runs.  Every width, ragged k, special values and padding columns:
+@pytest.mark.parametrize("m,n,k,s,seed", [(40, 300, 4000, 14, 11), (70, 257, 8100, 12, 12),
+                                          (33, 130, 16384, 16, 13), (20, 70, 16400, 14, 14)])
+def test_scale_split_matches_the_oracle_at_every_width(oz, m, n, k, s, seed):
+    A, B = hpl_like(m, n, k, phi=1.0, seed=seed)
+    B[:, 3] = 0.0                                   # an empty column
+    B[5, 7] = 2.0**-1070                            # a subnormal, and a column led by one
+    B[:, 9] = 0.0
+    B[123, 9] = -(2.0**-1060)
+    B[17, 11] = np.inf                              # a non-finite column
+    ref = O.prepare(A, B, s)
+    cc, kA, EA, EB, d, e, Apv, Bpv = ref
+    dA, dB = dev(A), dev(B)
+    rowexp, colexp, Ap, Bp = oz.ozaki2_scale_split(dA, dB, s)
+    assert np.array_equal(rowexp.cpu().numpy(), exps_as_int32(EA))
+    assert np.array_equal(colexp.cpu().numpy(), exps_as_int32(EB))
+    Bi = bf16_planes_to_int(Bp)
+    want = np.transpose(O.residue_planes(Bpv, cc.moduli), (0, 2, 1)).astype(np.int64)
+    ok_cols = [j for j in range(n) if EB[j] != "nan"]  # a non-finite column's planes are not used
+    assert np.array_equal(Bi[:, ok_cols, :k], want[:, ok_cols, :])
+    assert not Bi[:, n:, :].any() and not Bi[:, :, k:].any()
+    Ai = bf16_planes_to_int(Ap)
+    assert np.array_equal(Ai[:, :m, :k], O.residue_planes(Apv, cc.moduli).astype(np.int64))
+    assert oz.ozaki_get_device_status() == oz.OZ_OK
