@@ -54,11 +54,10 @@ def main():
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for _ in range(a.reps):
         ev[0].record()
-        if sc == oz.OZ_SCALE_UNIFORM:  # as ozaki2_scale_split runs steps a1 + a2 (B in one pass)
-            rc = lib.ozaki2_exponents(m, 0, k, p(dA), m, None, 1, p(rowexp), None, st)
+        if sc == oz.OZ_SCALE_UNIFORM:  # steps a1 + a2 together (timed as "split"; "exponents" is 0)
+            rc = 0
             ev[1].record()
-            rc |= lib.ozaki2_split(m, 0, k, p(dA), m, None, 1, s, p(rowexp), None, p(Ap), None, st)
-            rc |= lib.ozaki2_scale_split(0, n, k, None, 1, p(dB), k, s, None, p(colexp), None, p(Bp), st)
+            rc |= lib.ozaki2_scale_split(m, n, k, p(dA), m, p(dB), k, s, p(rowexp), p(colexp), p(Ap), p(Bp), st)
         else:
             rc = lib.ozaki2_exponents_ex(m, n, k, p(dA), m, p(dB), k, s, sc, p(rowexp), p(colexp), p(ews), nb, st)
             ev[1].record()

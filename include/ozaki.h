@@ -102,9 +102,11 @@ int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B,
 
 /* Steps a1 and a2 together (Algorithm 1 steps 2-3, left half): the exponents of
  * ozaki2_exponents and the planes of ozaki2_split, same arguments, layouts and errors, in
- * fewer passes over DRAM: each column of B is read from DRAM once (its maximum, then its
- * residues, the second read served by L2); A takes the two passes.  Either operand may be
- * skipped with NULL for its source, exponents and planes. */
+ * fewer passes over DRAM and with the two operands' passes overlapped: while Kp <= 16384
+ * each column of B is read from DRAM once (its maximum, then its residues, the second read
+ * served by L2), and B's passes run on a second stream of the library beside A's exponent pass
+ * and split, joined back to `stream` before the call's work on `stream` continues.  Either
+ * operand may be skipped with NULL for its source, exponents and planes. */
 int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                        int num_moduli, int32_t* rowexp, int32_t* colexp, uint16_t* A_planes,
                        uint16_t* B_planes, cudaStream_t stream);
