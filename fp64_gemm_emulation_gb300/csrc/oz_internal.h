@@ -29,6 +29,8 @@ struct SplitConsts {
   uint32_t c64[kMaxModuli];     // 2^64 mod m
   uint32_t c80[kMaxModuli];     // 2^80 mod m
   uint32_t magic[kMaxModuli];   // ceil(2^39 / m): y mod m for y < 2^30
+  uint32_t offs[kMaxModuli];    // m 2^22 + floor(m/2): the offset of the single Barrett step
+  uint32_t fbase[kMaxModuli];   // 0x4B000080 - floor(m/2): float bits of 2^23 + 128, shifted
   int shift_ok;                 // every modulus m has m 2^22 > 2^26 (the shifted path's bound)
 };
 

@@ -215,10 +215,12 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
       sx1[x] = sg * static_cast<int>(x1[x]);
       sx2[x] = sg * static_cast<int>(x2[x]);
     }
-#pragma unroll 1
-    for (int t = 0; t < c.s; ++t) {
+    // moduli unrolled: every constant is an operand at a fixed place of the parameter bank
+#pragma unroll
+    for (int t = 0; t < kMaxModuli; ++t) {
+      if (t >= c.s) break;
       const uint32_t m = static_cast<uint32_t>(c.mod[t]), c16 = c.c16[t], c32 = c.c32[t], mg = c.magic[t];
-      const uint32_t halfm = m >> 1, offs = (m << 22) + halfm, fbase = 0x4B000080u - halfm;
+      const uint32_t offs = c.offs[t], fbase = c.fbase[t];
       uint32_t w[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
@@ -247,7 +249,7 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
 }
 
 template <bool kRowsContiguous>
-__global__ void __launch_bounds__(kSplitThreads) split_kernel(int rows, int K, const double* __restrict__ X,
+__global__ void __launch_bounds__(kSplitThreads, 4) split_kernel(int rows, int K, const double* __restrict__ X,
                                                               long long rs, long long ks,
                                                               const int32_t* __restrict__ exps,
                                                               const SplitConsts c, uint16_t* __restrict__ planes,

@@ -158,6 +158,8 @@ int fill_split_consts(int s, long long k_inner, SplitConsts* out) {
     out->c64[t] = static_cast<uint32_t>((static_cast<uint64_t>(out->c48[t]) * out->c16[t]) % m);
     out->c80[t] = static_cast<uint32_t>((static_cast<uint64_t>(out->c64[t]) * out->c16[t]) % m);
     out->magic[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
+    out->offs[t] = (m << 22) + (m >> 1);
+    out->fbase[t] = 0x4B000080u - (m >> 1);
   }
   return OZ_OK;
 }
