@@ -288,7 +288,7 @@ static int crt_limbs(const CrtConsts& c) {
 cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const uint8_t* C_res,
                        const int32_t* rowexp, const int32_t* colexp, double* C, int ldc, cudaStream_t stream) {
   if (m == 0 || n == 0) return cudaSuccess;
-  dim3 grid((m + 1023) / 1024, n < 65535 ? n : 65535);
+  dim3 grid((m + 1023) / 1024, n < 1024 ? n : 1024);  // each block loops over n / 1024 columns
   const int nl = crt_limbs(c) < 3 ? 3 : crt_limbs(c);
   // 2^(32 (nl - 1)) / M: the quotient estimate reads the top limb in units of 2^(32 (nl - 1))
   double Md = 0.0;
