@@ -84,53 +84,114 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLim
   return bits | (neg ? 0x8000000000000000ull : 0ull);
 }
 
-// RN-even of (-1)^neg * x * 2^-D (x: NL limbs) for results that are normal numbers or
-// overflow, from 64-bit words: the word holding the leading one and the word below it
-// give the 64-bit window, anything lower only the sticky bit.  Returns false for results
-// in the subnormal range (the general routine above handles them).
+struct Words6 {
+  uint32_t w[kLimbs];
+};
+
+// The rare results in the subnormal range, out of line so that the common path keeps its
+// words in registers.
+__device__ __noinline__ uint64_t round_subnormal(Words6 v, bool neg, int D) {
+  return round_scaled_bits(v.w, neg, D);
+}
+
+// The CRT sum, range reduction and rounding of one element from its exact sum
+// Z = x[0..NL-1] (32-bit words, little-endian): returns the bits of C_ij.  All on 32-bit
+// words: the quotient estimate, X = Z - Q M (Q M from chained 32 x 32 -> 64-bit
+// multiply-adds), the magnitude, and the rounding from a 64-bit window cut out of the
+// three words from the leading one down (funnel shifts), the words below only as sticky.
 template <int NL>
-__device__ __forceinline__ bool round_normal_words(const uint32_t (&x)[kLimbs], bool neg, int D, uint64_t& out) {
-  constexpr int NW = (NL + 1) / 2;
-  uint64_t w[NW];
+__device__ __forceinline__ uint64_t crt_finish(uint32_t (&x)[kLimbs], int E, int F, const CrtConsts& c,
+                                               float inv_m_top) {
+  if (E == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) return 0x7FF8000000000000ull;
+  if (E == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) return 0;
+  // Q = floor(Z/M + 1/2 - 2^-8) from the top three words in FP32 (error < 2^-9):
+  // round(Z/M) or one less, never more, so X = Z - Q M is the representative or the
+  // representative plus M.  It is one less only if the estimate h lies within
+  // 2^-9 + 2^-8 of the next integer, so below a fractional part of 1 - 2^-7 it is
+  // exactly round(Z/M) and X needs no correction.
+  float zs = __uint2float_rn(x[NL - 1]);
+  zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, zs);
+  zs = fmaf(__uint2float_rn(x[NL - 3]), 5.421010862427522e-20f, zs);
+  const float h = fmaf(zs, inv_m_top, 0.49609375f);
+  const float hq = floorf(h);
+  const bool near = (h - hq) >= 0.9921875f;  // exact difference: h < 2^13
+  const uint32_t Q = static_cast<uint32_t>(hq);
+  {
+    uint32_t qc = 0, borrow = 0;
 #pragma unroll
-  for (int i = 0; i < NW; ++i)
-    w[i] = static_cast<uint64_t>(x[2 * i]) | ((2 * i + 1 < NL) ? static_cast<uint64_t>(x[2 * i + 1]) << 32 : 0ull);
-  // the highest non-zero word w[h] (h = 0 if all above w[0] are zero), the word below it, and
-  // whether any word further down is non-zero
-  uint64_t hi = w[0], lo = 0, below = 0;
-  int base = 0;
-#pragma unroll
-  for (int i = 1; i < NW; ++i) {
-    if (w[i] != 0) {
-      hi = w[i];
-      lo = w[i - 1];
-      base = 64 * i;
-      below = 0;
-#pragma unroll
-      for (int b = 0; b + 1 < i; ++b) below |= w[b];
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
+      qc = static_cast<uint32_t>(qm >> 32);
+      const uint64_t d = static_cast<uint64_t>(x[l]) - static_cast<uint32_t>(qm) - borrow;
+      x[l] = static_cast<uint32_t>(d);
+      borrow = static_cast<uint32_t>(d >> 32) & 1u;
     }
   }
-  bool sticky = below != 0;
-  if (hi == 0) {
-    out = 0;  // exact zero: +0.0
-    return true;
+  bool neg = (x[NL - 1] >> 31) != 0;
+  {  // magnitude: X for X >= 0, two's complement negation otherwise
+    const uint32_t flip = neg ? 0xFFFFFFFFu : 0u;
+    uint32_t cy = neg ? 1u : 0u;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+      const uint64_t v = static_cast<uint64_t>(x[l] ^ flip) + cy;
+      x[l] = static_cast<uint32_t>(v);
+      cy = static_cast<uint32_t>(v >> 32);
+    }
   }
-  const int lz = __clzll(static_cast<long long>(hi));
-  const uint64_t win = lz ? (hi << lz) | (lo >> (64 - lz)) : hi;
-  sticky = sticky || ((lz ? (lo << lz) : lo) != 0);
-  const int e_unb = base + 63 - lz - D;  // exponent of the leading one in the result
-  if (e_unb < -1022) return false;
-  const uint64_t sgn = neg ? 0x8000000000000000ull : 0ull;
-  if (e_unb > 1023) {
-    out = 0x7FF0000000000000ull | sgn;
-    return true;
+  if (near && !neg) {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
+    bool gt = false, decided = false;
+#pragma unroll
+    for (int l = NL - 1; l >= 0; --l) {
+      if (!decided && x[l] != c.halfM[l]) {
+        gt = x[l] > c.halfM[l];
+        decided = true;
+      }
+    }
+    if (gt) {
+      uint32_t b = 0;
+#pragma unroll
+      for (int l = 0; l < NL; ++l) {
+        const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
+        x[l] = static_cast<uint32_t>(d);
+        b = static_cast<uint32_t>(d >> 32) & 1u;
+      }
+      neg = true;
+    }
   }
-  uint64_t mant = win >> 11;
-  const bool rb = (win >> 10) & 1u;
-  sticky = sticky || ((win & 0x3FFu) != 0);
-  if (rb && (sticky || (mant & 1u))) ++mant;  // may carry into 2^53: exponent + 1 below
-  out = ((static_cast<uint64_t>(e_unb + 1022) << 52) + mant) | sgn;
-  return true;
+  const int D = 2 * c.kA - E - F;  // d_i + e_j
+  // leading word a = x[hi], then b, c below it; any word further down only as sticky
+  int hw = 0;
+  uint32_t a = x[0], b = 0, cw = 0, below = 0;
+#pragma unroll
+  for (int l = 1; l < NL; ++l) {
+    if (x[l] != 0) {
+      hw = l;
+      a = x[l];
+      b = x[l - 1];
+      cw = (l >= 2) ? x[l - 2] : 0u;
+      below = 0;
+#pragma unroll
+      for (int q = 0; q + 2 < l; ++q) below |= x[q];
+    }
+  }
+  if (a == 0) return 0;  // exact zero: +0.0
+  const int lz = __clz(a);
+  const uint32_t w1 = __funnelshift_l(b, a, lz);   // window bits 63..32 (leading one at bit 63)
+  const uint32_t w0 = __funnelshift_l(cw, b, lz);  // window bits 31..0
+  const bool sticky = ((cw << lz) | below | (w0 & 0x3FFu)) != 0;
+  const int e_unb = 32 * hw + 31 - lz - D;  // exponent of the leading one in the result
+  if (e_unb < -1022) {  // subnormal range: the general routine
+#pragma unroll
+    for (int l = NL; l < kLimbs; ++l) x[l] = 0;
+    return round_subnormal(Words6{x[0], x[1], x[2], x[3], x[4], x[5]}, neg, D);
+  }
+  const uint32_t sgn = neg ? 0x80000000u : 0u;
+  if (e_unb > 1023) return static_cast<uint64_t>(0x7FF00000u | sgn) << 32;
+  uint32_t mlo = __funnelshift_r(w0, w1, 11), mhi = w1 >> 11;  // 53-bit significand
+  const uint32_t inc = ((w0 >> 10) & 1u) & ((sticky ? 1u : 0u) | (mlo & 1u));
+  const uint64_t m = ((static_cast<uint64_t>(mhi) << 32) | mlo) + inc;  // may carry into 2^53: exponent + 1
+  const uint64_t bits = (static_cast<uint64_t>(e_unb + 1022) << 52) + m;
+  return bits | (static_cast<uint64_t>(sgn) << 32);
 }
 
 // One thread = 4 consecutive rows i of one column j (a 4-byte load per modulus).
@@ -194,14 +255,6 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (i0 + e >= m) break;
-      if (E[e] == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) {
-        out[e] = __longlong_as_double(0x7FF8000000000000ll);
-        continue;
-      }
-      if (E[e] == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) {
-        out[e] = 0.0;
-        continue;
-      }
       // Z into NL words: word w holds limbs 2w and 2w + 1; run < 2^29 + 2^45 + 2^32.
       uint32_t x[kLimbs];
       uint64_t run = 0;
@@ -212,65 +265,9 @@ __global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, 
         x[w] = static_cast<uint32_t>(run);
         run >>= 32;
       }
-      // Q = floor(Z/M + 1/2 - 2^-8) from the top three limbs in FP32 (error < 2^-9):
-      // round(Z/M) or one less, never more, so X = Z - Q M is the representative or
-      // the representative plus M.  It is one less only if the estimate h lies within
-      // 2^-9 + 2^-8 of the next integer, so below a fractional part of 1 - 2^-7 it is
-      // exactly round(Z/M) and X needs no correction.
-      float zs = __uint2float_rn(x[NL - 1]);
-      zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, zs);
-      zs = fmaf(__uint2float_rn(x[NL - 3]), 5.421010862427522e-20f, zs);
-      const float h = fmaf(zs, inv_m_top, 0.49609375f);
-      const float hq = floorf(h);
-      const bool near = (h - hq) >= 0.9921875f;  // exact difference: h < 2^13
-      const uint32_t Q = static_cast<uint32_t>(hq);
-      uint64_t qc = 0;
-      uint32_t borrow = 0;
 #pragma unroll
-      for (int l = 0; l < NL; ++l) {
-        const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
-        qc = qm >> 32;
-        const uint64_t d = static_cast<uint64_t>(x[l]) - static_cast<uint32_t>(qm) - borrow;
-        x[l] = static_cast<uint32_t>(d);
-        borrow = static_cast<uint32_t>(d >> 63);
-      }
-      bool neg = (x[NL - 1] >> 31) != 0;
-      {  // magnitude: X for X >= 0, two's complement negation otherwise
-        const uint32_t flip = neg ? 0xFFFFFFFFu : 0u;
-        uint32_t cy = neg ? 1u : 0u;
-#pragma unroll
-        for (int l = 0; l < NL; ++l) {
-          const uint64_t v = static_cast<uint64_t>(x[l] ^ flip) + cy;
-          x[l] = static_cast<uint32_t>(v);
-          cy = static_cast<uint32_t>(v >> 32);
-        }
-      }
-      if (near && !neg) {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
-        bool gt = false, decided = false;
-#pragma unroll
-        for (int l = NL - 1; l >= 0; --l) {
-          if (!decided && x[l] != c.halfM[l]) {
-            gt = x[l] > c.halfM[l];
-            decided = true;
-          }
-        }
-        if (gt) {
-          uint32_t b = 0;
-#pragma unroll
-          for (int l = 0; l < NL; ++l) {
-            const uint64_t d = static_cast<uint64_t>(c.M[l]) - x[l] - b;
-            x[l] = static_cast<uint32_t>(d);
-            b = static_cast<uint32_t>(d >> 63);
-          }
-          neg = true;
-        }
-      }
-#pragma unroll
-      for (int l = NL; l < kLimbs; ++l) x[l] = 0;
-      const int D = 2 * c.kA - E[e] - F;  // d_i + e_j
-      uint64_t bits;
-      if (!round_normal_words<NL>(x, neg, D, bits)) bits = round_scaled_bits(x, neg, D);
-      out[e] = __longlong_as_double(static_cast<long long>(bits));
+      for (int w = NL; w < kLimbs; ++w) x[w] = 0;
+      out[e] = __longlong_as_double(static_cast<long long>(crt_finish<NL>(x, E[e], F, c, inv_m_top)));
     }
   }
 }
