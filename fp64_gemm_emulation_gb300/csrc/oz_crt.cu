@@ -203,7 +203,7 @@ __device__ __forceinline__ uint64_t crt_finish(uint32_t (&x)[kLimbs], int E, int
 // moduli for one element come from a 4 x 4 byte transpose of the four elements' words.
 // The limbs are then carried into NL words.
 template <int NL, int N16>
-__global__ void __launch_bounds__(256) crt_kernel(int m, int n, int mp, int np, const CrtConsts c, float inv_m_top,
+__global__ void __launch_bounds__(256, 3) crt_kernel(int m, int n, int mp, int np, const CrtConsts c, float inv_m_top,
                                                   const uint8_t* __restrict__ C_res,
                                                   const int32_t* __restrict__ rowexp,
                                                   const int32_t* __restrict__ colexp, double* __restrict__ C,
