@@ -369,8 +369,8 @@ def run_ours(args, world, rank, local):
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        # steps a1 + a2 (ozaki2_scale_split: B's one-pass exponents and split with A's exponent
-        # pass beside it on a second stream, then A's split), the GEMM, the CRT
+        # steps a1 + a2 (ozaki2_scale_split: B's one-pass exponents and split, then A's exponent
+        # pass and split), the GEMM, the CRT
         rc = lib.ozaki2_scale_split(M, N, K, ptr(dA), M, ptr(dB), K, S, ptr(rowexp), ptr(colexp), ptr(Ap), ptr(Bp),
                                     sh)
         if ev:

@@ -8,7 +8,6 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 
 #include "oz_internal.h"
 
@@ -470,23 +469,6 @@ int ozaki2_split_ex(int m, int n, int k, const double* A, int lda, const double*
 // Longest padded k for which B's exponents and split take one DRAM pass.
 constexpr int kFusedMaxKp = 16384;
 
-// A second stream per device for work that runs beside the caller's stream inside one call
-// (created once, non-blocking, kept for the process; forked from and joined back to the
-// caller's stream with events, which stream capture records as graph dependencies).
-cudaStream_t side_stream() {
-  constexpr int kMaxDev = 64;
-  static std::mutex mu;
-  static cudaStream_t streams[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!streams[dev] && cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking) != cudaSuccess) {
-    cudaGetLastError();
-    streams[dev] = nullptr;
-  }
-  return streams[dev];
-}
-
 int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb, int num_moduli,
                        int32_t* rowexp, int32_t* colexp, uint16_t* A_planes, uint16_t* B_planes,
                        cudaStream_t stream) {
@@ -497,40 +479,23 @@ int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const doub
   SplitConsts sc;
   int rc = fill_split_consts(num_moduli, k, &sc);
   if (rc) return rc;
-  const bool doA = A && m > 0, doB = B && n > 0;
   const int np = static_cast<int>(roundup(n, kPadN)), kp = static_cast<int>(roundup(k, kPadK));
-  // B's steps run on a second stream beside A's: every pass here is bound by HBM, the splits
-  // by their plane writes, and neither operand's passes alone reach the write rate of the
-  // memory, so the two operands' passes overlap.  B takes one DRAM pass (each column's
-  // maximum, then its residues, the second read from L2) while a column fits in L2 many times
-  // over (Kp <= 16384: the resident blocks hold about 40 MB of columns); above that, the
-  // exponent pass and the split.
-  cudaStream_t side = (doA && doB) ? side_stream() : nullptr;
-  cudaStream_t sb = side ? side : stream;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  if (side && (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
-               cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess ||
-               cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess)) {
-    cudaGetLastError();
-    rc = OZ_ECUDA;
-  }
-  if (!rc && doB) {
+  // B: one DRAM pass (each column's maximum, then its residues, the second read from L2) while
+  // a column fits in L2 many times over (Kp <= 16384: the resident blocks hold about 40 MB of
+  // columns); above that, the exponent pass and the split.  A: the exponent pass, then the split.
+  if (B && n > 0) {
     if (kp <= kFusedMaxKp) {
-      rc = cuda_rc(launch_split_fused_kcontig(n, k, B, ldb, sc, colexp, B_planes, np, kp, sb));
+      rc = cuda_rc(launch_split_fused_kcontig(n, k, B, ldb, sc, colexp, B_planes, np, kp, stream));
     } else {
-      rc = ozaki2_exponents(0, n, k, nullptr, 1, B, ldb, nullptr, colexp, sb);
-      if (!rc) rc = ozaki2_split(0, n, k, nullptr, 1, B, ldb, num_moduli, nullptr, colexp, nullptr, B_planes, sb);
+      rc = ozaki2_exponents(0, n, k, nullptr, 1, B, ldb, nullptr, colexp, stream);
+      if (!rc) rc = ozaki2_split(0, n, k, nullptr, 1, B, ldb, num_moduli, nullptr, colexp, nullptr, B_planes, stream);
     }
+    if (rc) return rc;
   }
-  if (!rc && doA) rc = ozaki2_exponents(m, 0, k, A, lda, nullptr, 1, rowexp, nullptr, stream);
-  if (!rc && doA) rc = ozaki2_split(m, 0, k, A, lda, nullptr, 1, num_moduli, rowexp, nullptr, A_planes, nullptr, stream);
-  if (fork && join &&
-      (cudaEventRecord(join, side) != cudaSuccess || cudaStreamWaitEvent(stream, join, 0) != cudaSuccess)) {
-    cudaGetLastError();
-    if (!rc) rc = OZ_ECUDA;
+  if (A && m > 0) {
+    if ((rc = ozaki2_exponents(m, 0, k, A, lda, nullptr, 1, rowexp, nullptr, stream))) return rc;
+    rc = ozaki2_split(m, 0, k, A, lda, nullptr, 1, num_moduli, rowexp, nullptr, A_planes, nullptr, stream);
   }
-  if (fork) cudaEventDestroy(fork);
-  if (join) cudaEventDestroy(join);
   return rc;
 }
 

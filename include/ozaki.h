@@ -102,15 +102,10 @@ int ozaki2_split(int m, int n, int k, const double* A, int lda, const double* B,
 
 /* Steps a1 and a2 together (Algorithm 1 steps 2-3, left half): the exponents of
  * ozaki2_exponents and the planes of ozaki2_split, same arguments, layouts and errors, in
- * fewer passes over DRAM and with the two operands' passes overlapped: while Kp <= 16384
- * each column of B is read from DRAM once (its maximum, then its residues, the second read
- * served by L2), and B's passes run on a second stream of the library beside A's exponent pass
- * and split, joined back to `stream` before the call's work on `stream` continues.  The second
- * stream is one per device, created on first use and kept: calls from several host threads at
- * once stay correct, their B passes taking turns on it.  The fork and join are events, so a
- * call captured into a CUDA graph records them as graph dependencies (make one call before the
- * first capture, so that the stream exists).  Either operand may be skipped with NULL for its
- * source, exponents and planes. */
+ * fewer passes over DRAM: while Kp <= 16384 each column of B is read from DRAM once (its
+ * maximum, then its residues, the second read served by L2); A, and B at larger k, take the
+ * exponent pass and the split.  Everything is ordered on `stream`.  Either operand may be
+ * skipped with NULL for its source, exponents and planes. */
 int ozaki2_scale_split(int m, int n, int k, const double* A, int lda, const double* B, int ldb,
                        int num_moduli, int32_t* rowexp, int32_t* colexp, uint16_t* A_planes,
                        uint16_t* B_planes, cudaStream_t stream);
