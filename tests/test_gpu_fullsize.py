@@ -3,8 +3,8 @@
 At these sizes the oracle cannot compute all of C, so sampled entries are
 computed one by one from the definition (full row of A, full column of B, exact
 integers) and compared bit for bit; the rest of C is checked through properties
-that hold at any size (finite, NaN-free, and within the benchmark spec's bound of the
-float64 product's own error envelope on sampled rows).
+that hold at any size (finite, NaN-free, and within the float64 product's own error
+envelope).
 """
 import numpy as np
 import pytest

@@ -2,8 +2,8 @@
 
 Bar: bit-exact everywhere.  Exponents, residue planes and C''_t are integer data;
 the final C is the single rounding of an exact integer, which both sides take
-the same way, so C is compared bit for bit as well (the benchmark spec's tolerance
-|dC| <= 2^-50 (|A||B|) is checked on top as a sanity bound).
+the same way, so C is compared bit for bit as well (the tolerance
+|dC| <= 2^-50 (|A||B|) stated for the emulated product is checked on top as a sanity bound).
 """
 from fractions import Fraction
 
@@ -120,7 +120,7 @@ def test_dgemm_bit_exact(oz, m, n, k, s, phi, seed):
     ref = O.ozaki2_dgemm(A, B, s, keep=False).C
     C = oz.ozaki2_dgemm(dev(A), dev(B), s)
     assert np.array_equal(bits(host(C)), bits(ref))
-    # The spec floor |dC| <= 2^-50 (|A||B|) is about GPU vs oracle: dC = 0 here.
+    # The stated tolerance |dC| <= 2^-50 (|A||B|) is about GPU vs oracle: dC = 0 here.
     # Against the exact product, the error must stay inside the truncation bound
     # 2^-(d_i+e_j) sum_k (|a'_ik| + |b'_kj| + 1) plus half an ulp (sampled entries).
     cc, kA, EA, EB, d, e, Ap, Bp = O.prepare(A, B, s)
