@@ -32,6 +32,13 @@ struct SplitConsts {
   uint32_t offs[kMaxModuli];    // m 2^22 + floor(m/2): the offset of the single Barrett step
   uint32_t fbase[kMaxModuli];   // 0x4B000080 - floor(m/2): float bits of 2^23 + 128, shifted
   int shift_ok;                 // every modulus m has m 2^22 > 2^26 (the shifted path's bound)
+  // The 13-bit limb path (a' < 2^52 as four 13-bit limbs, FP32 arithmetic):
+  float f13[kMaxModuli];        // 2^13 mod m, 2^26 mod m, 2^39 mod m
+  float f26[kMaxModuli];
+  float f39[kMaxModuli];
+  float finv[kMaxModuli];       // 1/m rounded to FP32
+  float fmod[kMaxModuli];       // m
+  int limb13_ok;                // m_0 = 256 and every other modulus odd, in (128, 256)
 };
 
 // Constants of the CRT reconstruction (a5, a6).

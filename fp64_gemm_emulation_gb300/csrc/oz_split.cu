@@ -2,15 +2,16 @@
 //
 // [Ozaki II] Algorithm 1, step 2 (A' = trunc(DA)) and the left half of step 3
 // (A'_t = A' mod m_t, symmetric, signed 8-bit) for every modulus t, in one pass over
-// the FP64 operand.  Integer bit manipulation only (the FP64 units are not used):
-// a' = trunc(|a| 2^d) is kept as u * 2^p with u < 2^53, and a' mod m is
-// (u mod m)(2^p mod m) mod m with u split into 16-bit limbs.
+// the FP64 operand, without the FP64 units.  In the common case (a' < 2^52, no
+// power-of-two factor) a' is cut into four 13-bit limbs held as exact FP32 values and
+// each residue takes a few FP32 FMAs; otherwise a' = trunc(|a| 2^d) is kept as u * 2^p
+// with u < 2^53, and a' mod m is (u mod m)(2^p mod m) mod m with u split into 16-bit
+// limbs and one integer Barrett step.
 //
-// One block handles a 64 x 64 tile (rows x k).  Phase 1 reads the tile with
-// coalesced loads along whichever index is contiguous in memory and stores the
-// packed (sign, p, u) words in shared memory; phase 2 reads them along k and writes
-// 16-byte vectors of 8 bf16 residues per modulus, so the K-contiguous planes are
-// written in full 128-byte rows.
+// For a row-contiguous operand one block handles a 64 x 64 tile (rows x k): phase 1 reads
+// the tile with coalesced loads along the rows and stores the FP64 patterns in shared
+// memory; phase 2 reads them along k and writes 16-byte vectors of 8 bf16 residues per
+// modulus, so the K-contiguous planes are written in full 128-byte rows.
 #include "oz_fp.cuh"
 #include "oz_internal.h"
 
@@ -248,6 +249,108 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
   }
 }
 
+// ---------------------------------------------------------------- 13-bit limb path
+// The common case: every a' of the warp is u < 2^52 with no power-of-two factor (for
+// E = ceil(log2 max|a|) this holds whenever k_A <= 51, e.g. 14 moduli at every k >= 256).
+// Then a' = sign * (x0 + x1 2^13 + x2 2^26 + x3 2^39) with 13-bit limbs x_l, and for an odd
+// modulus 128 < m < 256
+//   y = sign * (x0 + x1 (2^13 mod m) + x2 (2^26 mod m) + x3 (2^39 mod m)) ≡ a' (mod m),
+// |y| <= 8191 (1 + 3 * 254) < 2^23, so y and every partial sum are exact in FP32.
+// q = round(y/m) from one FMA with 1/m rounded to FP32 (error |y| |1/m - fl(1/m)| < 2^23 2^-32
+// = 2^-9, below the distance 1/(2m) > 2^-9 from y/m to a half-integer, which holds for odd
+// m), and r = y - q m (exact) is the symmetric representative in [-(m-1)/2, (m-1)/2].
+// For m_0 = 256, y = sign * x0 (2^13 ≡ 0) and q = round((y + 1/4) / 256) (exact, never a
+// tie) takes r into [-128, 127].  Every step is an FP32 FMA or add: no integer multiply.
+// A zero limb, sum or remainder is +0 (an exact zero sum rounds to +0), so r's bf16 bits
+// are those of the integer residue.
+
+// Right shift that takes the 53-bit significand of x (exponent field raised to 1 for
+// zeros and subnormals) to trunc(|x| 2^(k_A - E)); rb = 1075 + E - k_A for the row.
+__device__ __forceinline__ int limb_shift(uint64_t raw, int rb) {
+  const int ex = static_cast<int>(static_cast<uint32_t>(raw >> 52) & 0x7FFu);
+  return rb - max(ex, 1);
+}
+
+// The row's rb: a row without finite nonzero entries (or a padding row) gets a shift that
+// clears every value, as the residues of such rows are zero.
+__device__ __forceinline__ int row_shift_base(int E, int kA) {
+  return (E == OZ_EXP_EMPTY || E == OZ_EXP_NONFINITE) ? 4096 : 1075 + E - kA;
+}
+
+// The four signed limbs of one value as exact floats (rs >= 1, so u < 2^52).
+__device__ __forceinline__ void limbs13(uint64_t raw, int rs, float (&x)[4]) {
+  const uint32_t lo = static_cast<uint32_t>(raw), hi = static_cast<uint32_t>(raw >> 32);
+  const uint32_t ex = (hi >> 20) & 0x7FFu;
+  const uint32_t hm = (hi & 0xFFFFFu) | (ex != 0 ? 0x100000u : 0u);  // significand bits 32..52
+  const int sh = min(rs, 63);
+  const bool low = sh < 32;
+  const uint32_t ul = low ? __funnelshift_r(lo, hm, sh) : (hm >> (sh & 31));
+  const uint32_t uh = low ? (hm >> sh) : 0u;
+  // sign * (2^23 + x) -/+ 2^23: exactly sign * x, and +0 for x = 0
+  const uint32_t sbit = hi & 0x80000000u;
+  const float sg = __uint_as_float(sbit | 0x3F800000u);
+  const float nb = __uint_as_float(sbit ^ 0xCB000000u);
+  x[0] = fmaf(__uint_as_float((ul & 0x1FFFu) | 0x4B000000u), sg, nb);
+  x[1] = fmaf(__uint_as_float(((ul >> 13) & 0x1FFFu) | 0x4B000000u), sg, nb);
+  x[2] = fmaf(__uint_as_float((__funnelshift_r(ul, uh, 26) & 0x1FFFu) | 0x4B000000u), sg, nb);
+  x[3] = fmaf(__uint_as_float((uh >> 7) | 0x4B000000u), sg, nb);
+}
+
+// Residues of 8 values (raw FP64 patterns of one row, rb its shift base) modulo every
+// modulus, 8 bf16 per plane at dst + t * plane_elems.  Every lane of the warp calls it;
+// returns false, having written nothing, unless every value of the warp has rs >= 1 (the
+// caller then takes the general path).  Lanes with dst == nullptr compute but do not store.
+__device__ __forceinline__ bool residues13_to_planes(const uint64_t (&raw)[8], int rb, const SplitConsts& c,
+                                                   uint16_t* dst, long long plane_elems) {
+  int rs[8];
+  int rmin = 1 << 30;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    rs[x] = limb_shift(raw[x], rb);
+    rmin = min(rmin, rs[x]);
+  }
+  if (!__all_sync(0xFFFFFFFFu, rmin >= 1)) return false;
+  float xl[8][4];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) limbs13(raw[x], rs[x], xl[x]);
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds |v| < 2^22 to an integer
+#pragma unroll
+  for (int t = 0; t < kMaxModuli; ++t) {
+    if (t >= c.s) break;
+    float r[8];
+    if (t == 0) {  // m = 256
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float q = fmaf(xl[x][0] + 0.25f, 0.00390625f, kMagic) - kMagic;
+        r[x] = fmaf(-q, 256.0f, xl[x][0]);
+      }
+    } else {
+      const float c1 = c.f13[t], c2 = c.f26[t], c3 = c.f39[t], iv = c.finv[t], mf = c.fmod[t];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const float y = fmaf(xl[x][3], c3, fmaf(xl[x][2], c2, fmaf(xl[x][1], c1, xl[x][0])));
+        const float q = fmaf(y, iv, kMagic) - kMagic;
+        r[x] = fmaf(-q, mf, y);
+      }
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) w[x] = __byte_perm(__float_as_uint(r[2 * x]), __float_as_uint(r[2 * x + 1]), 0x7632);
+    if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return true;
+}
+
+// 8 values of one row: the 13-bit limb path when it applies, the general path otherwise.
+__device__ __forceinline__ void split8(const uint64_t (&raw)[8], int E, const SplitConsts& c, uint16_t* dst,
+                                       long long plane_elems) {
+  if (c.limb13_ok && residues13_to_planes(raw, row_shift_base(E, c.kA), c, dst, plane_elems)) return;
+  uint64_t v[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) v[x] = pack_scaled(__longlong_as_double(static_cast<long long>(raw[x])), E, c.kA);
+  residues_to_planes(v, c, dst, plane_elems);
+}
+
 template <bool kRowsContiguous>
 __global__ void __launch_bounds__(kSplitThreads, 4) split_kernel(int rows, int K, const double* __restrict__ X,
                                                               long long rs, long long ks,
@@ -270,9 +373,8 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_kernel(int rows, int K
       r = (tid >> 6) + 4 * it;
     }
     const int gr = r0 + r, gk = k0 + kk;
-    uint64_t packed = 0;
-    if (gr < rows && gk < K) packed = pack_scaled(__ldg(X + gr * rs + gk * ks), __ldg(exps + gr), c.kA);
-    tile[kk][r] = packed;
+    tile[kk][r] = (gr < rows && gk < K) ? static_cast<uint64_t>(__double_as_longlong(__ldg(X + gr * rs + gk * ks)))
+                                        : 0ull;  // +0.0 outside the operand
   }
   __syncthreads();
 
@@ -285,8 +387,9 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_kernel(int rows, int K
     uint64_t v[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) v[x] = tile[g * 8 + x][r];
+    const int E = (r0 + r < rows) ? __ldg(exps + r0 + r) : OZ_EXP_EMPTY;
     uint16_t* dst = planes + static_cast<long long>(r0 + r) * kp + k0 + g * 8;
-    residues_to_planes(v, c, dst, plane_elems);
+    split8(v, E, c, dst, plane_elems);
   }
 }
 
@@ -303,17 +406,18 @@ __global__ void __launch_bounds__(256, 4) split_kcontig_kernel(int rows, int K, 
   const int r = valid ? static_cast<int>(item / groups) : 0;
   const int k0 = valid ? static_cast<int>(item - static_cast<long long>(r) * groups) * 8 : 0;
   uint64_t v[8];
+  int E = OZ_EXP_EMPTY;
   if (valid && r < rows) {
-    const int E = __ldg(exps + r);
+    E = __ldg(exps + r);
     const double* src = X + static_cast<long long>(r) * ld + k0;
 #pragma unroll
-    for (int x = 0; x < 8; ++x) v[x] = (k0 + x < K) ? pack_scaled(__ldg(src + x), E, c.kA) : 0ull;
+    for (int x = 0; x < 8; ++x) v[x] = (k0 + x < K) ? static_cast<uint64_t>(__double_as_longlong(__ldg(src + x))) : 0ull;
   } else {
 #pragma unroll
     for (int x = 0; x < 8; ++x) v[x] = 0;
   }
-  residues_to_planes(v, c, valid ? planes + static_cast<long long>(r) * kp + k0 : nullptr,
-                     static_cast<long long>(rows_padded) * kp);
+  split8(v, E, c, valid ? planes + static_cast<long long>(r) * kp + k0 : nullptr,
+         static_cast<long long>(rows_padded) * kp);
 }
 
 // Steps a1 + a2 for a K-contiguous operand (B: column j is k contiguous) with one DRAM read
@@ -352,8 +456,11 @@ __global__ void __launch_bounds__(kFusedThreads, 3)
     const int k0 = 8 * g;
     uint64_t v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (r < rows && g < groups && k0 + e < K) ? pack_scaled(__ldg(src + k0 + e), E, c.kA) : 0ull;
-    residues_to_planes(v, c, g < groups ? planes + static_cast<long long>(r) * kp + k0 : nullptr, plane_elems);
+    for (int e = 0; e < 8; ++e)
+      v[e] = (r < rows && g < groups && k0 + e < K) ? static_cast<uint64_t>(__double_as_longlong(__ldg(src + k0 + e)))
+                                                    : 0ull;
+    split8(v, r < rows ? E : OZ_EXP_EMPTY, c, g < groups ? planes + static_cast<long long>(r) * kp + k0 : nullptr,
+           plane_elems);
   }
 }
 

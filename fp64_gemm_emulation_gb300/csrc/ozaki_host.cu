@@ -159,7 +159,15 @@ int fill_split_consts(int s, long long k_inner, SplitConsts* out) {
     out->magic[t] = static_cast<uint32_t>(((1ull << 39) + m - 1) / m);
     out->offs[t] = (m << 22) + (m >> 1);
     out->fbase[t] = 0x4B000080u - (m >> 1);
+    out->f13[t] = static_cast<float>((1u << 13) % m);
+    out->f26[t] = static_cast<float>((1u << 26) % m);
+    out->f39[t] = static_cast<float>((1ull << 39) % m);
+    out->finv[t] = 1.0f / static_cast<float>(m);  // correctly rounded FP32 division
+    out->fmod[t] = static_cast<float>(m);
   }
+  out->limb13_ok = (s >= 1 && p.mod[0] == 256) ? 1 : 0;
+  for (int t = 1; t < s; ++t)
+    if (p.mod[t] % 2 == 0 || p.mod[t] <= 128 || p.mod[t] >= 256) out->limb13_ok = 0;
   return OZ_OK;
 }
 
