@@ -84,6 +84,133 @@ __device__ __forceinline__ uint64_t round_scaled_bits(const uint32_t (&mag)[kLim
   return bits | (neg ? 0x8000000000000000ull : 0ull);
 }
 
+// Multi-word arithmetic on NL little-endian 32-bit words with the carry flag (one asm
+// block per operation, so that no other instruction comes between the links of a chain).
+
+// x = a + b (mod 2^(32 NL)).
+template <int NL>
+__device__ __forceinline__ void add_words(uint32_t (&x)[kLimbs], const uint32_t (&a)[kLimbs],
+                                          const uint32_t (&b)[kLimbs]) {
+  if constexpr (NL == 3) {
+    asm("add.cc.u32 %0, %3, %6;\n\t"
+        "addc.cc.u32 %1, %4, %7;\n\t"
+        "addc.u32 %2, %5, %8;"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(b[0]), "r"(b[1]), "r"(b[2]));
+  } else if constexpr (NL == 4) {
+    asm("add.cc.u32 %0, %4, %8;\n\t"
+        "addc.cc.u32 %1, %5, %9;\n\t"
+        "addc.cc.u32 %2, %6, %10;\n\t"
+        "addc.u32 %3, %7, %11;"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]));
+  } else if constexpr (NL == 5) {
+    asm("add.cc.u32 %0, %5, %10;\n\t"
+        "addc.cc.u32 %1, %6, %11;\n\t"
+        "addc.cc.u32 %2, %7, %12;\n\t"
+        "addc.cc.u32 %3, %8, %13;\n\t"
+        "addc.u32 %4, %9, %14;"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]));
+  } else if constexpr (NL == 6) {
+    asm("add.cc.u32 %0, %6, %12;\n\t"
+        "addc.cc.u32 %1, %7, %13;\n\t"
+        "addc.cc.u32 %2, %8, %14;\n\t"
+        "addc.cc.u32 %3, %9, %15;\n\t"
+        "addc.cc.u32 %4, %10, %16;\n\t"
+        "addc.u32 %5, %11, %17;"
+        : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3]), "=r"(x[4]), "=r"(x[5])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]));
+  }
+}
+
+// x = x + cy (mod 2^(32 NL)), cy in {0, 1}.
+template <int NL>
+__device__ __forceinline__ void inc_words(uint32_t (&x)[kLimbs], uint32_t cy) {
+  if constexpr (NL == 3) {
+    asm("add.cc.u32 %0, %0, %3;\n\t"
+        "addc.cc.u32 %1, %1, 0;\n\t"
+        "addc.u32 %2, %2, 0;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2])
+        : "r"(cy));
+  } else if constexpr (NL == 4) {
+    asm("add.cc.u32 %0, %0, %4;\n\t"
+        "addc.cc.u32 %1, %1, 0;\n\t"
+        "addc.cc.u32 %2, %2, 0;\n\t"
+        "addc.u32 %3, %3, 0;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3])
+        : "r"(cy));
+  } else if constexpr (NL == 5) {
+    asm("add.cc.u32 %0, %0, %5;\n\t"
+        "addc.cc.u32 %1, %1, 0;\n\t"
+        "addc.cc.u32 %2, %2, 0;\n\t"
+        "addc.cc.u32 %3, %3, 0;\n\t"
+        "addc.u32 %4, %4, 0;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4])
+        : "r"(cy));
+  } else if constexpr (NL == 6) {
+    asm("add.cc.u32 %0, %0, %6;\n\t"
+        "addc.cc.u32 %1, %1, 0;\n\t"
+        "addc.cc.u32 %2, %2, 0;\n\t"
+        "addc.cc.u32 %3, %3, 0;\n\t"
+        "addc.cc.u32 %4, %4, 0;\n\t"
+        "addc.u32 %5, %5, 0;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5])
+        : "r"(cy));
+  }
+}
+
+// x = x + Q Mn (mod 2^(32 NL)): the products' low words in one carry chain, their high
+// words (one word up) in a second.
+template <int NL>
+__device__ __forceinline__ void mad_words(uint32_t (&x)[kLimbs], uint32_t Q, const uint32_t (&Mn)[kLimbs]) {
+  if constexpr (NL == 3) {
+    asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\t"
+        "madc.lo.cc.u32 %1, %3, %5, %1;\n\t"
+        "madc.lo.u32 %2, %3, %6, %2;\n\t"
+        "mad.hi.cc.u32 %1, %3, %4, %1;\n\t"
+        "madc.hi.u32 %2, %3, %5, %2;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2])
+        : "r"(Q), "r"(Mn[0]), "r"(Mn[1]), "r"(Mn[2]));
+  } else if constexpr (NL == 4) {
+    asm("mad.lo.cc.u32 %0, %4, %5, %0;\n\t"
+        "madc.lo.cc.u32 %1, %4, %6, %1;\n\t"
+        "madc.lo.cc.u32 %2, %4, %7, %2;\n\t"
+        "madc.lo.u32 %3, %4, %8, %3;\n\t"
+        "mad.hi.cc.u32 %1, %4, %5, %1;\n\t"
+        "madc.hi.cc.u32 %2, %4, %6, %2;\n\t"
+        "madc.hi.u32 %3, %4, %7, %3;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3])
+        : "r"(Q), "r"(Mn[0]), "r"(Mn[1]), "r"(Mn[2]), "r"(Mn[3]));
+  } else if constexpr (NL == 5) {
+    asm("mad.lo.cc.u32 %0, %5, %6, %0;\n\t"
+        "madc.lo.cc.u32 %1, %5, %7, %1;\n\t"
+        "madc.lo.cc.u32 %2, %5, %8, %2;\n\t"
+        "madc.lo.cc.u32 %3, %5, %9, %3;\n\t"
+        "madc.lo.u32 %4, %5, %10, %4;\n\t"
+        "mad.hi.cc.u32 %1, %5, %6, %1;\n\t"
+        "madc.hi.cc.u32 %2, %5, %7, %2;\n\t"
+        "madc.hi.cc.u32 %3, %5, %8, %3;\n\t"
+        "madc.hi.u32 %4, %5, %9, %4;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4])
+        : "r"(Q), "r"(Mn[0]), "r"(Mn[1]), "r"(Mn[2]), "r"(Mn[3]), "r"(Mn[4]));
+  } else if constexpr (NL == 6) {
+    asm("mad.lo.cc.u32 %0, %6, %7, %0;\n\t"
+        "madc.lo.cc.u32 %1, %6, %8, %1;\n\t"
+        "madc.lo.cc.u32 %2, %6, %9, %2;\n\t"
+        "madc.lo.cc.u32 %3, %6, %10, %3;\n\t"
+        "madc.lo.cc.u32 %4, %6, %11, %4;\n\t"
+        "madc.lo.u32 %5, %6, %12, %5;\n\t"
+        "mad.hi.cc.u32 %1, %6, %7, %1;\n\t"
+        "madc.hi.cc.u32 %2, %6, %8, %2;\n\t"
+        "madc.hi.cc.u32 %3, %6, %9, %3;\n\t"
+        "madc.hi.cc.u32 %4, %6, %10, %4;\n\t"
+        "madc.hi.u32 %5, %6, %11, %5;"
+        : "+r"(x[0]), "+r"(x[1]), "+r"(x[2]), "+r"(x[3]), "+r"(x[4]), "+r"(x[5])
+        : "r"(Q), "r"(Mn[0]), "r"(Mn[1]), "r"(Mn[2]), "r"(Mn[3]), "r"(Mn[4]), "r"(Mn[5]));
+  }
+}
+
 struct Words6 {
   uint32_t w[kLimbs];
 };
@@ -96,47 +223,34 @@ __device__ __noinline__ uint64_t round_subnormal(Words6 v, bool neg, int D) {
 
 // The CRT sum, range reduction and rounding of one element from its exact sum
 // Z = x[0..NL-1] (32-bit words, little-endian): returns the bits of C_ij.  All on 32-bit
-// words: the quotient estimate, X = Z - Q M (Q M from chained 32 x 32 -> 64-bit
-// multiply-adds), the magnitude, and the rounding from a 64-bit window cut out of the
-// three words from the leading one down (funnel shifts), the words below only as sticky.
+// words: the quotient estimate, X = Z - Q M (as Z + Q (2^(32 NL) - M) in two carry
+// chains), the magnitude, and the rounding from a 64-bit window cut out of the three words
+// from the leading one down (funnel shifts), the words below only as sticky.
 template <int NL>
 __device__ __forceinline__ uint64_t crt_finish(uint32_t (&x)[kLimbs], int E, int F, const CrtConsts& c,
                                                float inv_m_top) {
   if (E == OZ_EXP_NONFINITE || F == OZ_EXP_NONFINITE) return 0x7FF8000000000000ull;
   if (E == OZ_EXP_EMPTY || F == OZ_EXP_EMPTY) return 0;
-  // Q = floor(Z/M + 1/2 - 2^-8) from the top three words in FP32 (error < 2^-9):
+  // z = Z/M - 2^-8 in FP32 from the top two words, all three when NL = 3 (error below
+  // 2^-10: Z/M < 255 s < 2^13, a few roundings of relative size 2^-24 and one of 2^-13; for
+  // NL >= 4, M > 2^83 and the words left out are worth less than 2^-18).  Q = round(z) is
   // round(Z/M) or one less, never more, so X = Z - Q M is the representative or the
-  // representative plus M.  It is one less only if the estimate h lies within
-  // 2^-9 + 2^-8 of the next integer, so below a fractional part of 1 - 2^-7 it is
-  // exactly round(Z/M) and X needs no correction.
-  float zs = __uint2float_rn(x[NL - 1]);
-  zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, zs);
-  zs = fmaf(__uint2float_rn(x[NL - 3]), 5.421010862427522e-20f, zs);
-  const float h = fmaf(zs, inv_m_top, 0.49609375f);
-  const float hq = floorf(h);
-  const bool near = (h - hq) >= 0.9921875f;  // exact difference: h < 2^13
-  const uint32_t Q = static_cast<uint32_t>(hq);
-  {
-    uint32_t qc = 0, borrow = 0;
-#pragma unroll
-    for (int l = 0; l < NL; ++l) {
-      const uint64_t qm = static_cast<uint64_t>(Q) * c.M[l] + qc;
-      qc = static_cast<uint32_t>(qm >> 32);
-      const uint64_t d = static_cast<uint64_t>(x[l]) - static_cast<uint32_t>(qm) - borrow;
-      x[l] = static_cast<uint32_t>(d);
-      borrow = static_cast<uint32_t>(d >> 32) & 1u;
-    }
-  }
+  // representative plus M.  It is one less only if Z/M lies just above a half-integer,
+  // where z lies within 2^-8 + 2^-10 below it: every such element has |z - Q| > 0.4921875,
+  // and only those elements compare X with M/2.
+  float zs = fmaf(__uint2float_rn(x[NL - 2]), 2.3283064365386963e-10f, __uint2float_rn(x[NL - 1]));
+  if constexpr (NL == 3) zs = fmaf(__uint2float_rn(x[0]), 5.421010862427522e-20f, zs);
+  const float z = fmaf(zs, inv_m_top, -0.00390625f);
+  const float t = z + 8388608.0f;  // 2^23 + round(z), as -0.5 < z < 2^13
+  const uint32_t Q = __float_as_uint(t) - 0x4B000000u;
+  const bool near = fabsf(z - (t - 8388608.0f)) > 0.4921875f;  // exact difference
+  mad_words<NL>(x, Q, c.Mneg);                                   // X = Z - Q M (mod 2^(32 NL))
   bool neg = (x[NL - 1] >> 31) != 0;
   {  // magnitude: X for X >= 0, two's complement negation otherwise
     const uint32_t flip = neg ? 0xFFFFFFFFu : 0u;
-    uint32_t cy = neg ? 1u : 0u;
 #pragma unroll
-    for (int l = 0; l < NL; ++l) {
-      const uint64_t v = static_cast<uint64_t>(x[l] ^ flip) + cy;
-      x[l] = static_cast<uint32_t>(v);
-      cy = static_cast<uint32_t>(v >> 32);
-    }
+    for (int l = 0; l < NL; ++l) x[l] ^= flip;
+    inc_words<NL>(x, flip & 1u);
   }
   if (near && !neg) {  // X > M/2 means X = representative + M, representative < 0: magnitude M - X
     bool gt = false, decided = false;
@@ -255,18 +369,19 @@ __global__ void __launch_bounds__(256, 3) crt_kernel(int m, int n, int mp, int n
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (i0 + e >= m) break;
-      // Z into NL words: word w holds limbs 2w and 2w + 1; run < 2^29 + 2^45 + 2^32.
-      uint32_t x[kLimbs];
-      uint64_t run = 0;
+      // Z into NL words: word w = limb 2w + limb 2w+1 shifted up by 16 (its low half; the
+      // high half of limb 2w-1 joins it) in one carry chain.  Z < 2^(32 NL), so the top
+      // limb is below 2^16 and no carry leaves the top word.
+      uint32_t x[kLimbs], ev[kLimbs], od[kLimbs];
 #pragma unroll
-      for (int w = 0; w < NL; ++w) {
-        if (2 * w < N16) run += acc[e][2 * w];
-        if (2 * w + 1 < N16) run += static_cast<uint64_t>(acc[e][2 * w + 1]) << 16;
-        x[w] = static_cast<uint32_t>(run);
-        run >>= 32;
+      for (int w = 0; w < kLimbs; ++w) {
+        const uint32_t below = (w >= 1 && 2 * w - 1 < N16) ? acc[e][w >= 1 ? 2 * w - 1 : 0] : 0u;
+        const uint32_t above = (2 * w + 1 < N16) ? acc[e][2 * w + 1] : 0u;
+        ev[w] = (2 * w < N16) ? acc[e][2 * w] : 0u;
+        od[w] = __byte_perm(below, above, 0x5432);  // below >> 16 | (above & 0xFFFF) << 16
+        x[w] = 0;
       }
-#pragma unroll
-      for (int w = NL; w < kLimbs; ++w) x[w] = 0;
+      add_words<NL>(x, ev, od);
       out[e] = __longlong_as_double(static_cast<long long>(crt_finish<NL>(x, E[e], F, c, inv_m_top)));
     }
   }
@@ -291,9 +406,16 @@ cudaError_t launch_crt(int m, int n, int mp, int np, const CrtConsts& c, const u
   double Md = 0.0;
   for (int l = kLimbs - 1; l >= 0; --l) Md = Md * 4294967296.0 + c.M[l];
   const float inv_m_top = static_cast<float>(std::ldexp(1.0, 32 * (nl - 1)) / Md);
+  CrtConsts cc = c;  // with 2^(32 nl) - M for the quotient's subtraction
+  uint32_t borrow = 0;
+  for (int l = 0; l < kLimbs; ++l) {
+    const uint64_t d = (l < nl) ? 0ull - static_cast<uint64_t>(c.M[l]) - borrow : 0ull;
+    cc.Mneg[l] = (l < nl) ? static_cast<uint32_t>(d) : 0u;
+    borrow = (l < nl) ? static_cast<uint32_t>(d >> 63) : 0u;
+  }
   // (NL, N16) for each moduli count: the words of Z and the 16-bit limbs of M
 #define OZ_CRT_LAUNCH(NLv, N16v) \
-  crt_kernel<NLv, N16v><<<grid, 256, 0, stream>>>(m, n, mp, np, c, inv_m_top, C_res, rowexp, colexp, C, ldc)
+  crt_kernel<NLv, N16v><<<grid, 256, 0, stream>>>(m, n, mp, np, cc, inv_m_top, C_res, rowexp, colexp, C, ldc)
   switch (nl * 16 + c.n16) {
     case 3 * 16 + 1: OZ_CRT_LAUNCH(3, 1); break;
     case 3 * 16 + 2: OZ_CRT_LAUNCH(3, 2); break;

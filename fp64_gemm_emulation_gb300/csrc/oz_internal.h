@@ -52,6 +52,7 @@ struct CrtConsts {
   uint32_t Pd[kMaxModuli / 2][kHalfLimbs];
   uint32_t M[kLimbs];
   uint32_t halfM[kLimbs];          // floor(M / 2)
+  uint32_t Mneg[kLimbs];           // 2^(32 NL) - M for the launch's word count NL (set by launch_crt)
 };
 
 constexpr int kMaxPairs = OZ_MAX_SLICES * (OZ_MAX_SLICES + 1) / 2;  // Scheme I products
