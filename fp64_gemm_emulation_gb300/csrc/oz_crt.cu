@@ -3,16 +3,16 @@
 // [Ozaki II] Algorithm 1, steps 4-6.  Per output element, with residues
 // c_t = C''_t in [0, m_t) and P_t = M_t y_t (< M, so P_t / M = y_t / m_t):
 //   Z    = sum_t c_t P_t                      exact: 16-bit limb sums (dot products), then up to six words
-//   Q    = round(Z / M) or one less            from the top limbs of Z in FP32
+//   Q    = round(Z / M) or one less            from the top words of Z in FP32
 //   X    = Z - Q M, then one correction by M  symmetric representative, |X| < M/2
 //   C    = RN(X 2^-(d_i + e_j))               one rounding, subnormals included
-// The quotient estimate is biased down by 2^-8, more than its error, so it is never
-// too large and at most one too small; one correction then restores the unique
+// The quotient is rounded from Z/M - 2^-8, a bias larger than the estimate's error, so it
+// is never too large and at most one too small; one correction then restores the unique
 // representative ([Ozaki II] section 5: the true product lies in (-M/2, M/2) because
-// 2 c_max < M).  The estimate can only be one too small when its fractional part is
-// within 3 * 2^-9 of the next integer, so the comparison with M/2 that detects it runs
-// for those elements alone (X near +-M/2; none for typical products, whose |X| is far
-// below M/2).  The remainder and the rounding are exact integer arithmetic.
+// 2 c_max < M).  It can only be one too small when the biased estimate lies within
+// 2^-8 + 2^-10 below a half-integer, so the comparison with M/2 that detects it runs for
+// those elements alone (X near +-M/2; none for typical products, whose |X| is far below
+// M/2).  The remainder and the rounding are exact integer arithmetic.
 #include <cmath>
 
 #include "oz_internal.h"
