@@ -12,6 +12,10 @@ use no GPU and share no code with the kernels.
 * CRT quotient estimate: z = Z/M - 2^-8 is taken in FP32 from the top words of Z, and
   Q = round(z). Q is round(Z/M) or one less, never more. Every element where Q is one less
   is flagged by |z - Q| > 63/128.
+* CRT rounding: a 64-bit window is cut from the leading word down, with the words below
+  kept only as a sticky bit, then rounded to nearest-even and assembled with the exponent.
+  For normal results this equals the correctly rounded X 2^-D, at ties, near-ties, carries
+  into the next binade and overflow.
 """
 import math
 import random
@@ -165,3 +169,63 @@ def test_crt_quotient_estimate_is_never_too_large_and_flags_every_shortfall():
             r = (Z + M // 2) // M
             assert Q in (r, r - 1), (s, Z)
             assert Q == r or near, (s, Z)
+
+
+def _crt_round_model(X: int, nl: int, D: int):
+    """The CRT kernel's rounding of a magnitude X (nl 32-bit words) times 2^-D: the 64-bit
+    window from the leading word down, sticky bits below, RN-even, exponent assembly.
+    Returns the IEEE bits, or None where the kernel hands over to its subnormal routine."""
+    x = [(X >> (32 * w)) & 0xFFFFFFFF for w in range(nl)]
+    hw, a, b, cw, below = 0, x[0], 0, 0, 0
+    for l in range(1, nl):
+        if x[l]:
+            hw, a, b = l, x[l], x[l - 1]
+            cw = x[l - 2] if l >= 2 else 0
+            below = 0
+            for q in range(l - 2):
+                below |= x[q]
+    if a == 0:
+        return 0
+    lz = 32 - a.bit_length()
+    fsl = lambda lo, hi, sh: ((((hi << 32) | lo) << sh) >> 32) & 0xFFFFFFFF
+    w1, w0 = fsl(b, a, lz), fsl(cw, b, lz)
+    sticky = (((cw << lz) & 0xFFFFFFFF) | below | (w0 & 0x3FF)) != 0
+    e_unb = 32 * hw + 31 - lz - D
+    if e_unb < -1022:
+        return None
+    if e_unb > 1023:
+        return 0x7FF0000000000000
+    mlo = ((((w1 << 32) | w0) >> 11) & 0xFFFFFFFF)
+    mhi = w1 >> 11
+    inc = ((w0 >> 10) & 1) & (int(sticky) | (mlo & 1))
+    m = ((mhi << 32) | mlo) + inc
+    return (((e_unb + 1022) << 52) + m) & 0xFFFFFFFFFFFFFFFF
+
+
+def test_crt_rounding_window_is_round_to_nearest_even():
+    rng = random.Random(13)
+    handed_over = 0
+    for trial in range(20000):
+        nl = rng.choice([3, 4, 5, 6])
+        top = rng.randint(1, 32 * nl - 1)
+        X = rng.getrandbits(top) | (1 << top)  # leading one at bit `top`
+        X &= (1 << (32 * nl)) - 1
+        shape = rng.random()
+        if shape < 0.2 and top > 53:  # exact ties (half a last place, nothing below) and near-ties
+            cut = top - 52 - rng.choice([0, 1])
+            X = (X >> cut << cut) | (1 << (cut - 1))
+        elif shape < 0.3:  # carries through a run of ones
+            X = ((1 << (top + 1)) - 1) & ((1 << (32 * nl)) - 1)
+        D = rng.randint(-1100, 1300)
+        want_val = Fr(X) / Fr(2) ** D
+        got = _crt_round_model(X, nl, D)
+        if got is None:
+            handed_over += 1
+            assert want_val < Fr(2) ** -1022
+            continue
+        try:
+            want = _bits(float(want_val))  # Python rounds a Fraction to nearest, ties to even
+        except OverflowError:
+            want = 0x7FF0000000000000
+        assert got == want, (nl, top, D, hex(got), hex(want))
+    assert handed_over > 100
