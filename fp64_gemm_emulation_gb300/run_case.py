@@ -2,9 +2,9 @@
 
     python -m fp64_gemm_emulation_gb300.run_case --m 4096 --n 4096 --k 4096 --moduli 14 --reps 3
 
-Runs the four steps (exponents, split, residue GEMM, CRT) through the C ABI on
-HPL-like inputs resident on the GPU, ``--reps`` times, and prints per-step CUDA-event
-times of the last repetition.
+Runs the steps (exponents and split, as one ``ozaki2_scale_split`` call in the uniform
+scaling; residue GEMM; CRT) through the C ABI on HPL-like inputs resident on the GPU,
+``--reps`` times, and prints per-step CUDA-event times of the last repetition.
 """
 from __future__ import annotations
 
@@ -71,10 +71,14 @@ def main():
             raise SystemExit(f"ozaki call failed: {rc}")
     torch.cuda.synchronize()
     status = oz.ozaki_get_device_status()
-    names = ["exponents", "split", "residue_gemm", "crt"]
     t = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+    if sc == oz.OZ_SCALE_UNIFORM:  # steps a1 + a2 ran as one call
+        names, t = ["scale_split", "residue_gemm", "crt"], [t[0] + t[1], t[2], t[3]]
+    else:
+        names = ["exponents", "split", "residue_gemm", "crt"]
+    tg = t[names.index("residue_gemm")]
     print(f"{m}x{n}x{k} s={s} {a.scaling}: " + ", ".join(f"{nm} {x:.3f} ms" for nm, x in zip(names, t))
-          + f"; gemm {s * 2.0 * m * n * k / (t[2] * 1e-3) / 1e12:.1f} TFLOP/s; status {status}")
+          + f"; gemm {s * 2.0 * m * n * k / (tg * 1e-3) / 1e12:.1f} TFLOP/s; status {status}")
     if status:
         raise SystemExit(1)
     if a.graph:
