@@ -12,6 +12,8 @@ use no GPU and share no code with the kernels.
 * CRT quotient estimate: z = Z/M - 2^-8 is taken in FP32 from the top words of Z, and
   Q = round(z). Q is round(Z/M) or one less, never more. Every element where Q is one less
   is flagged by |z - Q| > 63/128.
+* Split, integer path: umulhi(ys, ceil(2^39 / m)) >> 7 is floor(ys / m) for every
+  0 <= ys < 2^31 (both ends of every run of equal quotients are checked).
 * CRT rounding: a 64-bit window is cut from the leading word down, with the words below
   kept only as a sticky bit, then rounded to nearest-even and assembled with the exponent.
   For normal results this equals the correctly rounded X 2^-D, at ties, near-ties, carries
@@ -229,3 +231,18 @@ def test_crt_rounding_window_is_round_to_nearest_even():
             want = 0x7FF0000000000000
         assert got == want, (nl, top, D, hex(got), hex(want))
     assert handed_over > 100
+
+
+def test_split_integer_barrett_step_is_exact_below_2_31():
+    # The split's integer path (a' with a power-of-two factor, or above 2^52) takes
+    # q = floor(ys / m) as umulhi(ys, ceil(2^39 / m)) >> 7 for 0 <= ys < 2^31.  The estimate
+    # is monotone in ys, so it is exact on every [k m, k m + m - 1] when it is exact at both
+    # ends; both ends are checked for every k.
+    for m in MODULI:
+        magic = -(-(1 << 39) // m)
+        assert magic < 1 << 32
+        k = np.arange(0, ((1 << 31) - 1) // m + 1, dtype=np.uint64)
+        for ys in (k * np.uint64(m), k * np.uint64(m) + np.uint64(m - 1)):
+            ys = ys[ys < np.uint64(1 << 31)]
+            q = ((ys * np.uint64(magic)) >> np.uint64(32)) >> np.uint64(7)
+            assert np.array_equal(q, ys // np.uint64(m)), m
