@@ -14,6 +14,8 @@ use no GPU and share no code with the kernels.
   is flagged by |z - Q| > 63/128.
 * Split, integer path: umulhi(ys, ceil(2^39 / m)) >> 7 is floor(ys / m) for every
   0 <= ys < 2^31 (both ends of every run of equal quotients are checked).
+* GEMM epilogue: q = RN(v fl32(1/m)) keeps every remainder v - q m of an exact chunk sum
+  below m in magnitude, and the 16-bit running lanes cannot overflow between reductions.
 * CRT rounding: a 64-bit window is cut from the leading word down, with the words below
   kept only as a sticky bit, then rounded to nearest-even and assembled with the exponent.
   For normal results this equals the correctly rounded X 2^-D, at ties, near-ties, carries
@@ -246,3 +248,19 @@ def test_split_integer_barrett_step_is_exact_below_2_31():
             ys = ys[ys < np.uint64(1 << 31)]
             q = ((ys * np.uint64(magic)) >> np.uint64(32)) >> np.uint64(7)
             assert np.array_equal(q, ys // np.uint64(m)), m
+
+
+def test_gemm_epilogue_quotient_keeps_every_remainder_below_m():
+    # The GEMM epilogue takes each exact chunk sum v (|v| <= 2^24) to r = v - q m with
+    # q = RN(v fl32(1/m)) (the 1.5 * 2^23 constant) and needs |r| < m.  q is monotone in v,
+    # so q(k m) = k for every k with |k m| < 2^25 puts q between floor(v/m) and ceil(v/m)
+    # for every v in range, hence |r| < m.
+    for m in MODULI:
+        n, e = _f32_as_ratio(np.float32(1.0) / np.float32(m))
+        k = np.arange(-((1 << 25) // m), (1 << 25) // m + 1, dtype=np.int64)
+        v = k * m
+        q = _round_half_even(v * n, e)
+        assert np.array_equal(q, k), m
+    # the 16-bit running lanes: a lane below m gains less than 2m per chunk, 64 chunks
+    # between reductions
+    assert 256 + 64 * (2 * 256 - 1) < 1 << 16
