@@ -79,7 +79,8 @@ __device__ __forceinline__ uint32_t residue_bf16(uint32_t x0, uint32_t x1, uint3
   return __float_as_uint(f) >> 16;
 }
 
-// Fast path (p == 0): the symmetric residue of a' = sign * u modulo m, as a float.
+// Integer path with p == 0 (a' = sign * u, u up to 2^53; the FP32 limb path below takes
+// u < 2^52): the symmetric residue of a' modulo m, as a float.
 //   ys = sign * (x2 c32 + x1 c16 + x0) + BIG + floor(m/2)   (BIG = m 2^22)
 //   q  = floor(ys / m)                                      (one Barrett step)
 //   ys - q m = v + floor(m/2) with v the symmetric representative in
@@ -140,9 +141,10 @@ __device__ __forceinline__ float residue_shifted(int sx0, int sx1, int sx2, int 
   return __int_as_float(static_cast<int>(fbase + (ys - q * m))) - 8388736.0f;
 }
 
-// Residues of the 8 packed values of one thread modulo every modulus, written as 8 bf16
-// (16 bytes) per plane at dst + t * plane_elems.  Every lane of the warp must call it
-// (the p == 0 test is warp-uniform); lanes with dst == nullptr compute but do not store.
+// The integer paths: residues of the 8 packed values of one thread modulo every modulus,
+// written as 8 bf16 (16 bytes) per plane at dst + t * plane_elems, for warps the FP32 limb
+// path does not take.  Every lane of the warp must call it (the p tests are warp-uniform);
+// lanes with dst == nullptr compute but do not store.
 __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const SplitConsts& c, uint16_t* dst,
                                                  long long plane_elems) {
   // per element: 16-bit limbs of u, the shift p and the sign, shared by all moduli
@@ -207,7 +209,7 @@ __device__ __forceinline__ void residues_to_planes(const uint64_t (&v)[8], const
       if (dst) *reinterpret_cast<uint4*>(dst + t * plane_elems) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   } else if (!warp_any_p) {
-    // common case: every a' of the warp is u itself (no power-of-two factor)
+    // every a' of the warp is u itself (no power-of-two factor), some u >= 2^52
     int sx0[8], sx1[8], sx2[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) {
